@@ -1,0 +1,459 @@
+#!/usr/bin/env python3
+"""Benchmark of the int8 (C8) paged KV-cache store + dequant-gather on GB300.
+
+One step = one store of a batch's new K/V tokens into the paged cache plus one
+dequant-gather of every sequence's full context (metadata plan + gather), i.e.
+the whole hot path, through the C ABI of libkvc8.
+
+Default workload: "prefill" -- batch 16, prompts U{512..4096} into an empty
+cache, 8 kv heads x head_dim 128, block 128, 1024-block pool, dynamic
+per-token scales, N(0,1) K/V with 4 outlier channels per head (x20).  Other
+workloads: --workload tiny|decode|mixed|longctx.
+
+Timing: W untimed warm-up steps, then exactly K steps.  L2 is flushed (a
+256 MiB write) before each timed kernel; each op is bracketed by CUDA events on
+the launching stream; the step time is the sum of its ops' event times.
+Barrier + synchronize on both sides; max over ranks.  SM clocks are sampled
+with nvidia-smi during the timed region.
+
+Printed: one JSON line (rank 0).  value = algorithmic HBM bytes of store +
+gather per step / step time, in GB/s; tokens/s and GB/s of each op are in
+"ops".  e2e = the same metric through the public API with the new tokens and
+metadata copied host->device and the gathered K/V copied device->host (pinned
+buffers) inside the timed region.  --impl reference times the CPU oracle
+instead (the reference arm: a plain single-threaded restatement of the method).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from dequant_kvc8_store_gb300 import workloads as W  # noqa: E402
+
+FALLBACK_HBM_GBS = 6800.0
+FLUSH_BYTES = 256 << 20
+METRIC = "achieved HBM GB/s (% of ~8 TB/s) and K+V tokens/s for store and dequant"
+KERNEL_SOURCES = ["dequant_kvc8_store_gb300/csrc/kvc8_store.cu",
+                  "dequant_kvc8_store_gb300/csrc/kvc8_gather.cu",
+                  "dequant_kvc8_store_gb300/csrc/kvc8_internal.cuh"]
+WORKLOAD_TEXT = {
+    "tiny": "tiny round trip: batch 2, q {5,19} after {3,0} cached, 2 kv heads x 64, block 16, "
+            "8 blocks, dynamic scales",
+    "prefill": "prefill store+gather: batch 16, prompts U[512,4096] into an empty cache, 8 kv "
+               "heads x 128, block 128, 1024-block pool, dynamic per-token scales, N(0,1) with "
+               "4 outlier channels/head x20",
+    "decode": "decode append + full-context gather: batch 256, 1 new token, cached U[1,8192], "
+              "8 x 128, block 128, 18000-block pool, dynamic scales",
+    "mixed": "chunked-prefill mix: 64 seqs (32 decode, 32 chunks U[256,2048]), cached "
+             "U[0,16384], 8 x 128, block 64, 20480-block pool, static scales U[0.005,0.05]",
+    "longctx": "long-context gather: 8 x 131072 cached tokens, 8 x 128, block 128, 8192 "
+               "blocks, dynamic scales U[0.01,0.1]",
+}
+
+
+def source_hash() -> str:
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def ncu_traffic(workload: str):
+    """Per-launch DRAM bytes of the dominant kernels from the committed ncu
+    summary, if it was taken on the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except Exception:
+        return {}
+    if d.get("source_hash") != source_hash():
+        return {}
+    return d.get("workloads", {}).get(workload, {})
+
+
+# ---------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling in a background process."""
+
+    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None, period_ms: int = 50):
+        self.uuid = uuid
+        self.period_ms = period_ms
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", str(self.period_ms)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                text=True)
+            self.reader = threading.Thread(target=self._read, daemon=True)
+            self.reader.start()
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.reader.join(timeout=2)
+
+    def summary(self):
+        rows = []
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            if self.uuid and parts[0] != self.uuid:
+                continue
+            rows.append(parts)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------- GPU arm
+
+def run_gpu(args, rank, world):
+    import torch
+    import dequant_kvc8_store_gb300 as kv
+    from dequant_kvc8_store_gb300.device import DeviceBatch
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    kv.load()
+    w = W.NAMED[args.workload](seed=1000 + list(W.NAMED).index(args.workload) + 7919 * rank)
+    nbytes = W.algorithmic_bytes(w)
+    d = DeviceBatch(w, device=dev)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    has_store = w.has_store and w.num_tokens > 0
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+
+    def step(e=None):
+        flush.fill_(1)
+        if e: e[0].record(stream)
+        if has_store:
+            d.store(stream)
+        if e: e[1].record(stream)
+        flush.fill_(2)
+        if e: e[2].record(stream)
+        d.build_metadata(stream=stream)
+        if e: e[3].record(stream)
+        d.gather_planned(stream)
+        if e: e[4].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    if d.error_code() != 0:
+        raise RuntimeError("device error during warm-up")
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    with ClockSampler(uuid) as clocks:
+        barrier()
+        t0 = time.perf_counter()
+        for i in range(args.steps):
+            step(ev[i])
+        barrier()
+        wall = time.perf_counter() - t0
+    st_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    plan_ms = [e[2].elapsed_time(e[3]) for e in ev]
+    ga_ms = [e[3].elapsed_time(e[4]) for e in ev]
+    step_ms = [a + b + c for a, b, c in zip(st_ms, plan_ms, ga_ms)]
+    if d.error_code() != 0:
+        raise RuntimeError("device error during the timed steps")
+    local = {"step_ms": float(np.mean(step_ms)), "store_ms": float(np.mean(st_ms)),
+             "plan_ms": float(np.mean(plan_ms)), "gather_ms": float(np.mean(ga_ms)),
+             "wall_s": wall}
+    if world > 1:
+        t = torch.tensor([local["step_ms"], local["store_ms"], local["gather_ms"]],
+                         dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        local["step_ms"], local["store_ms"], local["gather_ms"] = (float(x) for x in t.tolist())
+    e2e = run_e2e(args, w, d, dev, nbytes) if rank == 0 else None
+    return w, nbytes, local, clocks.summary(), e2e, has_store
+
+
+def run_e2e(args, w, d, dev, nbytes):
+    """Same step through the public API with host buffers: H2D of the new K/V
+    and the batch metadata from pinned memory, store, plan, gather, D2H of the
+    gathered K/V into pinned memory -- all inside the timed region."""
+    import torch
+    from dequant_kvc8_store_gb300.device import _bf16
+
+    stream = torch.cuda.current_stream()
+    host = {}
+    if d.k_states is not None:
+        host["k_states"] = _bf16(w.k_states).pin_memory()
+        host["v_states"] = _bf16(w.v_states).pin_memory()
+    host["block_table"] = torch.from_numpy(w.block_table).pin_memory()
+    if w.cu_q_lens is not None:
+        host["cu_q_lens"] = torch.from_numpy(w.cu_q_lens).pin_memory()
+    host["context_kv_lens"] = torch.from_numpy(w.context_kv_lens).pin_memory()
+    host["context_lengths"] = torch.from_numpy(w.context_lengths).pin_memory()
+    out_k = torch.empty(d.k_out.shape, dtype=torch.bfloat16).pin_memory()
+    out_v = torch.empty(d.v_out.shape, dtype=torch.bfloat16).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_k.numel() * 2 * 2
+    steps = max(3, min(args.steps, 50))
+
+    def step():
+        for name, t in host.items():
+            getattr(d, name).copy_(t, non_blocking=True)
+        d.store(stream)
+        d.gather(stream)
+        out_k.copy_(d.k_out, non_blocking=True)
+        out_v.copy_(d.v_out, non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    total = nbytes["store"] + nbytes["gather"]
+    return {"value": round(total / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "ms_per_step": round(ms, 4), "steps": steps}
+
+
+# ---------------------------------------------------------------------------- CPU arm
+
+def sub_workload(w: W.Workload, token_budget: int) -> W.Workload:
+    """The first sequences of a workload, the last one cut, holding about
+    token_budget stored + gathered positions: a bounded sample of it."""
+    import copy
+    s = copy.copy(w)
+    q = w.q_lens().astype(np.int64)
+    ctx0 = w.context_kv_lens.astype(np.int64)
+    keep_q, keep_c, used = [], [], 0
+    for b in range(w.num_seqs):
+        cost = int(q[b]) + int(ctx0[b] + q[b])
+        if used + cost > token_budget and keep_q:
+            break
+        keep_q.append(int(q[b]))
+        keep_c.append(int(ctx0[b]))
+        used += cost
+        if used >= token_budget:
+            break
+    B = len(keep_q)
+    if B == 1 and used > token_budget:  # cut the one sequence
+        frac = token_budget / max(used, 1)
+        keep_c[0] = int(keep_c[0] * frac)
+        keep_q[0] = max(0 if not w.has_store else 1, int(keep_q[0] * frac))
+        if not w.has_store:
+            keep_q[0] = 0
+    s.block_table = w.block_table[:B]
+    s.context_kv_lens = np.array(keep_c, np.int32)
+    s.context_lengths = (np.array(keep_c) + np.array(keep_q)).astype(np.int32)
+    if w.has_store:
+        n = int(sum(keep_q))
+        if w.cu_q_lens is not None:
+            s.cu_q_lens = np.concatenate([[0], np.cumsum(keep_q)]).astype(np.int32)
+        s.k_states = w.k_states[:n]
+        s.v_states = w.v_states[:n]
+    return s
+
+
+def oracle_pass(w: W.Workload):
+    import oracle
+    kc, vc = w.k_cache, w.v_cache
+    ks, vs = w.k_scale, w.v_scale
+    t0 = time.perf_counter()
+    if w.has_store:
+        oracle.store(w.quant_mode, w.k_states, w.v_states, kc, vc, ks, vs, w.block_table,
+                     w.cu_q_lens, w.context_kv_lens)
+    oracle.dequant_gather(w.quant_mode, kc, vc, ks, vs, w.block_table, w.context_lengths)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(w: W.Workload, seconds: float = 12.0, per_pass_cap: float = 3.0):
+    """The oracle as it stands on one host core, on a bounded sample of the
+    workload (whole passes when one pass is cheap enough)."""
+    full = int(w.q_lens().sum() + w.context_lengths.astype(np.int64).sum())
+    budget = full
+    s = w
+    # shrink the sample until one pass takes at most per_pass_cap seconds
+    probe = sub_workload(w, min(full, 20000))
+    t = oracle_pass(probe)
+    rate = (int(probe.q_lens().sum()) + int(probe.context_lengths.astype(np.int64).sum())) / max(t, 1e-9)
+    if full / rate > per_pass_cap:
+        budget = int(rate * per_pass_cap)
+        s = sub_workload(w, budget)
+    bytes_pass = sum(W.algorithmic_bytes(s).values())
+    times, t_end = [], time.perf_counter() + seconds
+    while time.perf_counter() < t_end or not times:
+        times.append(oracle_pass(s))
+    gbs = bytes_pass / statistics.median(times) / 1e9
+    sample = (f"{len(times)} oracle passes of {'the full workload' if s is w else 'its first %d sequences' % s.num_seqs} "
+              f"({int(s.q_lens().sum())} stored + {int(s.context_lengths.astype(np.int64).sum())} "
+              f"gathered positions, {bytes_pass / 1e6:.1f} MB algorithmic per pass), median pass")
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": sample}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    w = W.NAMED[args.workload](seed=1000 + list(W.NAMED).index(args.workload))
+    steps, warm = args.steps, args.warmup
+    # each step a bounded sample, sized so the whole run stays within ~2 minutes
+    per_step = min(2.0, 100.0 / max(1, steps + warm))
+    probe = sub_workload(w, 4000)
+    t = oracle_pass(probe)
+    rate = (int(probe.q_lens().sum()) + int(probe.context_lengths.astype(np.int64).sum())) / max(t, 1e-9)
+    s = sub_workload(w, max(64, int(rate * per_step)))
+    bytes_step = sum(W.algorithmic_bytes(s).values())
+    for _ in range(warm):
+        oracle_pass(s)
+    times = [oracle_pass(s) for _ in range(steps)]
+    ms = 1e3 * sum(times) / len(times)
+    value = bytes_step / (ms * 1e-3) / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": steps, "warmup": warm, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic", "config": {"workload": WORKLOAD_TEXT[args.workload],
+                                        "sample_positions_per_step": int(s.q_lens().sum() + s.context_lengths.astype(np.int64).sum())},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"each step: oracle store+gather of the first {s.num_seqs} "
+                                   f"sequences of the workload ({bytes_step / 1e6:.2f} MB algorithmic)"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["kvc8", "reference"], default="kvc8")
+    ap.add_argument("--workload", choices=list(W.NAMED), default="prefill")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        torch.distributed.init_process_group("nccl")
+    w, nbytes, t, clocks, e2e, has_store = run_gpu(args, rank, world)
+    if rank == 0:
+        peak, peak_kind = measured_peak()
+        total = nbytes["store"] + nbytes["gather"]
+        value = world * total / (t["step_ms"] * 1e-3) / 1e9
+        ops = {
+            "store": {"ms": round(t["store_ms"], 5),
+                      "GB_s": round(nbytes["store"] / (t["store_ms"] * 1e-3) / 1e9, 1) if has_store else None,
+                      "tokens_per_s": round(w.num_tokens / (t["store_ms"] * 1e-3), 1) if has_store else None,
+                      "bytes": nbytes["store"]},
+            "plan": {"ms": round(t["plan_ms"], 5)},
+            "dequant_gather": {"ms": round(t["gather_ms"], 5),
+                               "GB_s": round(nbytes["gather"] / (t["gather_ms"] * 1e-3) / 1e9, 1),
+                               "tokens_per_s": round(w.total_context / (t["gather_ms"] * 1e-3), 1),
+                               "bytes": nbytes["gather"]},
+        }
+        # the dominant kernel: the op with the larger device time
+        dom = "dequant_gather" if (t["gather_ms"] >= t["store_ms"] or not has_store) else "store"
+        dom_bytes = nbytes["gather"] if dom == "dequant_gather" else nbytes["store"]
+        dom_ms = t["gather_ms"] if dom == "dequant_gather" else t["store_ms"]
+        achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
+        traffic = ncu_traffic(args.workload).get("gather_kernel" if dom == "dequant_gather" else "store_kernel")
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t["step_ms"], 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD_TEXT[args.workload],
+                       "l2": "flushed (256 MiB write) before each timed op",
+                       "hbm_frac_of_step": round(total / (t["step_ms"] * 1e-3) / 1e9 / peak, 4),
+                       "tokens_per_s": {"store": ops["store"]["tokens_per_s"],
+                                        "dequant_gather": ops["dequant_gather"]["tokens_per_s"]}},
+            "ops": ops,
+            "roofline": {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1),
+                         "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                         "peak_kind": peak_kind, "traffic": traffic,
+                         "algorithmic_bytes": dom_bytes},
+            "gpu_launches": args.steps * (3 if has_store else 2),
+            "clocks": clocks,
+            "e2e": e2e,
+            "wall_s": round(t["wall_s"], 3),
+        }
+        if world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(w)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

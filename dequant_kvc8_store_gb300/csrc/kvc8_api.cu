@@ -1,0 +1,235 @@
+// kvc8_api.cu -- the extern "C" entry points of libkvc8 (declared in kvc8.h):
+// host-side argument checks, then the launches in kvc8_store.cu and
+// kvc8_gather.cu.  Nothing here allocates device memory or synchronises,
+// except kvc8_get_error, whose purpose is to synchronise.
+#include <cstdint>
+
+#include "kvc8_internal.cuh"
+
+namespace kvc8 {
+
+int sm_count() {
+    static int cached[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    if (dev < 64 && cached[dev] > 0) return cached[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+        n = 1;
+    if (dev < 64) cached[dev] = n;
+    return n;
+}
+
+namespace {
+
+constexpr int kMaxHeadDim = 256;
+constexpr int64_t kMaxStaticTable = 12288;  // kv_heads * head_dim, mode-1 store shared memory
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+kvc8_status check_geom(const kvc8_geom *g) {
+    if (g == nullptr) return KVC8_ERR_INVALID_ARG;
+    if (g->num_seqs < 0 || g->kv_heads < 1 || g->block_size < 1 || g->num_blocks < 1 ||
+        g->max_blocks_per_seq < 1 || g->head_dim < 16)
+        return KVC8_ERR_INVALID_ARG;
+    if (g->quant_mode != 0 && g->quant_mode != 1) return KVC8_ERR_INVALID_ARG;
+    if (g->head_dim % 16 != 0) return KVC8_ERR_INVALID_ARG;
+    if (g->head_dim > kMaxHeadDim) return KVC8_ERR_UNSUPPORTED;
+    // tile and unit counters are 32/64-bit; keep B * MB * 2H well inside int64
+    if ((int64_t)g->num_seqs * g->max_blocks_per_seq > (int64_t)INT32_MAX) return KVC8_ERR_UNSUPPORTED;
+    return KVC8_OK;
+}
+
+kvc8_status cuda_status(cudaError_t e) { return e == cudaSuccess ? KVC8_OK : KVC8_ERR_CUDA; }
+
+kvc8_status check_workspace(const kvc8_geom *g, const void *ws, size_t bytes) {
+    if (ws == nullptr || !aligned(ws, kAlign)) return KVC8_ERR_WORKSPACE;
+    if (bytes < plan_bytes(g->num_seqs)) return KVC8_ERR_WORKSPACE;
+    return KVC8_OK;
+}
+
+kvc8_status check_gather_args(const kvc8_geom *g, const int8_t *kc, const int8_t *vc,
+                              const float *ks, const float *vs, const int32_t *bt,
+                              const int32_t *lens, const void *ko, const void *vo,
+                              int64_t out_rows, int64_t tok_stride, int64_t head_stride) {
+    if (kc == nullptr || vc == nullptr || ks == nullptr || vs == nullptr || bt == nullptr ||
+        lens == nullptr || ko == nullptr || vo == nullptr)
+        return KVC8_ERR_INVALID_ARG;
+    if (out_rows < 0 || tok_stride < 0 || head_stride < 0) return KVC8_ERR_INVALID_ARG;
+    if (tok_stride % 8 != 0 || head_stride % 8 != 0) return KVC8_ERR_INVALID_ARG;
+    if (!aligned(ko, 16) || !aligned(vo, 16) || !aligned(kc, 16) || !aligned(vc, 16))
+        return KVC8_ERR_INVALID_ARG;
+    if (!aligned(ks, 16) || !aligned(vs, 16)) return KVC8_ERR_INVALID_ARG;
+    return KVC8_OK;
+}
+
+}  // namespace
+}  // namespace kvc8
+
+using namespace kvc8;
+
+extern "C" {
+
+const char *kvc8_status_str(kvc8_status s) {
+    switch (s) {
+        case KVC8_OK: return "ok";
+        case KVC8_ERR_INVALID_ARG: return "invalid argument";
+        case KVC8_ERR_UNSUPPORTED: return "unsupported geometry";
+        case KVC8_ERR_CUDA: return "CUDA error";
+        case KVC8_ERR_DEVICE_BOUNDS: return "device-side bounds error";
+        case KVC8_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
+    }
+    return "unknown status";
+}
+
+int32_t kvc8_version(void) { return 10000; }
+
+kvc8_status kvc8_store(const kvc8_geom *g, int64_t num_tokens, const void *key_states,
+                       const void *value_states, int64_t x_tok_stride, int64_t x_head_stride,
+                       int8_t *key_cache, int8_t *value_cache, float *key_scale,
+                       float *value_scale, const int32_t *block_table, const int32_t *cu_q_lens,
+                       const int32_t *context_kv_lens, int32_t *dev_error, cudaStream_t stream) {
+    kvc8_status st = check_geom(g);
+    if (st != KVC8_OK) return st;
+    if (num_tokens < 0) return KVC8_ERR_INVALID_ARG;
+    if (cu_q_lens == nullptr && num_tokens != g->num_seqs) return KVC8_ERR_INVALID_ARG;
+    if (num_tokens == 0 || g->num_seqs == 0) return num_tokens == 0 ? KVC8_OK : KVC8_ERR_INVALID_ARG;
+    if (key_states == nullptr || value_states == nullptr || key_cache == nullptr ||
+        value_cache == nullptr || key_scale == nullptr || value_scale == nullptr ||
+        block_table == nullptr || context_kv_lens == nullptr)
+        return KVC8_ERR_INVALID_ARG;
+    if (x_tok_stride < 0 || x_head_stride < 0 || x_tok_stride % 8 != 0 || x_head_stride % 8 != 0)
+        return KVC8_ERR_INVALID_ARG;
+    if (!aligned(key_states, 16) || !aligned(value_states, 16) || !aligned(key_cache, 8) ||
+        !aligned(value_cache, 8))
+        return KVC8_ERR_INVALID_ARG;
+    if (!aligned(key_scale, 16) || !aligned(value_scale, 16)) return KVC8_ERR_INVALID_ARG;
+    if (g->quant_mode == 1 && (int64_t)g->kv_heads * g->head_dim > kMaxStaticTable)
+        return KVC8_ERR_UNSUPPORTED;
+    StoreArgs a;
+    a.g = *g;
+    a.num_tokens = num_tokens;
+    a.k_states = static_cast<const uint16_t *>(key_states);
+    a.v_states = static_cast<const uint16_t *>(value_states);
+    a.x_tok_stride = x_tok_stride;
+    a.x_head_stride = x_head_stride;
+    a.k_cache = key_cache;
+    a.v_cache = value_cache;
+    a.k_scale = key_scale;
+    a.v_scale = value_scale;
+    a.block_table = block_table;
+    a.cu_q_lens = cu_q_lens;
+    a.context_kv_lens = context_kv_lens;
+    a.dev_error = dev_error;
+    return cuda_status(launch_store(a, stream));
+}
+
+size_t kvc8_gather_workspace_bytes(const kvc8_geom *g) {
+    if (g == nullptr || g->num_seqs < 0) return 0;
+    return plan_bytes(g->num_seqs);
+}
+
+kvc8_status kvc8_build_metadata(const kvc8_geom *g, const int32_t *context_lengths,
+                                const int64_t *context_seq_offset, int64_t *offsets_out,
+                                void *workspace, size_t workspace_bytes, int32_t *dev_error,
+                                cudaStream_t stream) {
+    kvc8_status st = check_geom(g);
+    if (st != KVC8_OK) return st;
+    if (context_lengths == nullptr && g->num_seqs > 0) return KVC8_ERR_INVALID_ARG;
+    st = check_workspace(g, workspace, workspace_bytes);
+    if (st != KVC8_OK) return st;
+    return cuda_status(launch_plan(*g, context_lengths, context_seq_offset, offsets_out,
+                                   workspace, dev_error, stream));
+}
+
+kvc8_status kvc8_dequant_gather(const kvc8_geom *g, const int8_t *key_cache,
+                                const int8_t *value_cache, const float *key_scale,
+                                const float *value_scale, const int32_t *block_table,
+                                const int32_t *context_lengths,
+                                const int64_t *context_seq_offset, void *key_out,
+                                void *value_out, int64_t out_rows, int64_t out_tok_stride,
+                                int64_t out_head_stride, void *workspace,
+                                size_t workspace_bytes, int32_t *dev_error,
+                                cudaStream_t stream) {
+    kvc8_status st = check_geom(g);
+    if (st != KVC8_OK) return st;
+    if (g->num_seqs == 0) return KVC8_OK;
+    st = check_gather_args(g, key_cache, value_cache, key_scale, value_scale, block_table,
+                           context_lengths, key_out, value_out, out_rows, out_tok_stride,
+                           out_head_stride);
+    if (st != KVC8_OK) return st;
+    st = check_workspace(g, workspace, workspace_bytes);
+    if (st != KVC8_OK) return st;
+    cudaError_t e = launch_plan(*g, context_lengths, context_seq_offset, nullptr, workspace,
+                                dev_error, stream);
+    if (e != cudaSuccess) return KVC8_ERR_CUDA;
+    GatherArgs a;
+    a.g = *g;
+    a.k_cache = key_cache;
+    a.v_cache = value_cache;
+    a.k_scale = key_scale;
+    a.v_scale = value_scale;
+    a.block_table = block_table;
+    a.context_lengths = context_lengths;
+    a.k_out = static_cast<uint16_t *>(key_out);
+    a.v_out = static_cast<uint16_t *>(value_out);
+    a.out_rows = out_rows;
+    a.out_tok_stride = out_tok_stride;
+    a.out_head_stride = out_head_stride;
+    a.plan = workspace;
+    a.dev_error = dev_error;
+    return cuda_status(launch_gather(a, /*use_pdl=*/true, stream));
+}
+
+kvc8_status kvc8_dequant_gather_planned(const kvc8_geom *g, const int8_t *key_cache,
+                                        const int8_t *value_cache, const float *key_scale,
+                                        const float *value_scale, const int32_t *block_table,
+                                        const int32_t *context_lengths, void *key_out,
+                                        void *value_out, int64_t out_rows,
+                                        int64_t out_tok_stride, int64_t out_head_stride,
+                                        const void *workspace, size_t workspace_bytes,
+                                        int32_t *dev_error, cudaStream_t stream) {
+    kvc8_status st = check_geom(g);
+    if (st != KVC8_OK) return st;
+    if (g->num_seqs == 0) return KVC8_OK;
+    st = check_gather_args(g, key_cache, value_cache, key_scale, value_scale, block_table,
+                           context_lengths, key_out, value_out, out_rows, out_tok_stride,
+                           out_head_stride);
+    if (st != KVC8_OK) return st;
+    st = check_workspace(g, workspace, workspace_bytes);
+    if (st != KVC8_OK) return st;
+    GatherArgs a;
+    a.g = *g;
+    a.k_cache = key_cache;
+    a.v_cache = value_cache;
+    a.k_scale = key_scale;
+    a.v_scale = value_scale;
+    a.block_table = block_table;
+    a.context_lengths = context_lengths;
+    a.k_out = static_cast<uint16_t *>(key_out);
+    a.v_out = static_cast<uint16_t *>(value_out);
+    a.out_rows = out_rows;
+    a.out_tok_stride = out_tok_stride;
+    a.out_head_stride = out_head_stride;
+    a.plan = workspace;
+    a.dev_error = dev_error;
+    return cuda_status(launch_gather(a, /*use_pdl=*/false, stream));
+}
+
+kvc8_status kvc8_get_error(int32_t *dev_error, int32_t *host_code, int32_t reset,
+                           cudaStream_t stream) {
+    if (dev_error == nullptr || host_code == nullptr) return KVC8_ERR_INVALID_ARG;
+    int32_t v = 0;
+    if (cudaMemcpyAsync(&v, dev_error, sizeof v, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+        return KVC8_ERR_CUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return KVC8_ERR_CUDA;
+    *host_code = v;
+    if (reset) {
+        if (cudaMemsetAsync(dev_error, 0, sizeof(int32_t), stream) != cudaSuccess)
+            return KVC8_ERR_CUDA;
+        if (cudaStreamSynchronize(stream) != cudaSuccess) return KVC8_ERR_CUDA;
+    }
+    return v == 0 ? KVC8_OK : KVC8_ERR_DEVICE_BOUNDS;
+}
+
+}  // extern "C"

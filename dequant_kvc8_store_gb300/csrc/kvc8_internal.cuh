@@ -1,0 +1,144 @@
+// kvc8_internal.cuh -- device helpers and launcher declarations shared by the
+// libkvc8 translation units (store, gather, C ABI).  Not part of the ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "kvc8.h"
+
+namespace kvc8 {
+
+// ---------------------------------------------------------------------------
+// Memory access helpers (inline PTX).
+
+// 16-byte read-once load: bypass L1 allocation, data is streamed.
+__device__ __forceinline__ uint4 ld_stream_16(const void *p) {
+    uint4 v;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+        : "l"(p));
+    return v;
+}
+
+// 4-byte read-only load through the non-coherent path (metadata, scales).
+__device__ __forceinline__ float ld_nc_f32(const float *p) {
+    float v;
+    asm("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ int32_t ld_nc_s32(const int32_t *p) {
+    int32_t v;
+    asm("ld.global.nc.s32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+
+// 8-byte store with default (write-back) caching: the cache pages are read
+// again by the consumer of the cache.
+__device__ __forceinline__ void st_8(void *p, uint32_t a, uint32_t b) {
+    asm volatile("st.global.v2.u32 [%0], {%1, %2};" ::"l"(p), "r"(a), "r"(b) : "memory");
+}
+
+// 16-byte streaming store (evict-first): write-once output.
+__device__ __forceinline__ void st_stream_16(void *p, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+    asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(a), "r"(b),
+                 "r"(c), "r"(d)
+                 : "memory");
+}
+
+// 32-byte streaming store (sm_100+ 256-bit vector store).
+__device__ __forceinline__ void st_stream_32(void *p, uint4 lo, uint4 hi) {
+    asm volatile("st.global.cs.v8.u32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p),
+                 "r"(lo.x), "r"(lo.y), "r"(lo.z), "r"(lo.w), "r"(hi.x), "r"(hi.y), "r"(hi.z),
+                 "r"(hi.w)
+                 : "memory");
+}
+
+// Programmatic dependent launch: let the next kernel on the stream start its
+// prologue, and wait for the previous kernel's results.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait_prior_grid() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// First device error wins; later ones are dropped.
+__device__ __forceinline__ void report(int32_t *dev_error, int32_t code) {
+    if (dev_error != nullptr) atomicCAS(dev_error, 0, code);
+}
+
+// ---------------------------------------------------------------------------
+// Gather plan, written by the plan kernel into the caller's workspace.
+//   header.total_tiles : number of (sequence, logical block) tiles
+//   offsets[B]         : first output row of each sequence (int64)
+//   tile_start[B + 1]  : exclusive prefix of ceil(len_b / bs), tile_start[B] = total
+struct PlanHeader {
+    int64_t total_tiles;
+    int64_t pad[3];
+};
+
+constexpr size_t kAlign = 256;
+
+__host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+__host__ __device__ inline size_t plan_offsets_at(int32_t) { return align_up(sizeof(PlanHeader), kAlign); }
+__host__ __device__ inline size_t plan_tile_start_at(int32_t num_seqs) {
+    return plan_offsets_at(num_seqs) + align_up(sizeof(int64_t) * (size_t)(num_seqs > 0 ? num_seqs : 1), kAlign);
+}
+__host__ __device__ inline size_t plan_bytes(int32_t num_seqs) {
+    return plan_tile_start_at(num_seqs) + align_up(sizeof(int32_t) * ((size_t)num_seqs + 1), kAlign);
+}
+
+// ---------------------------------------------------------------------------
+// Launchers (host).  Arguments are validated by the C ABI before these run.
+
+struct StoreArgs {
+    kvc8_geom g;
+    int64_t num_tokens;
+    const uint16_t *k_states;
+    const uint16_t *v_states;
+    int64_t x_tok_stride;
+    int64_t x_head_stride;
+    int8_t *k_cache;
+    int8_t *v_cache;
+    float *k_scale;
+    float *v_scale;
+    const int32_t *block_table;
+    const int32_t *cu_q_lens;
+    const int32_t *context_kv_lens;
+    int32_t *dev_error;
+};
+
+struct GatherArgs {
+    kvc8_geom g;
+    const int8_t *k_cache;
+    const int8_t *v_cache;
+    const float *k_scale;
+    const float *v_scale;
+    const int32_t *block_table;
+    const int32_t *context_lengths;
+    uint16_t *k_out;
+    uint16_t *v_out;
+    int64_t out_rows;
+    int64_t out_tok_stride;
+    int64_t out_head_stride;
+    const void *plan;
+    int32_t *dev_error;
+};
+
+cudaError_t launch_store(const StoreArgs &a, cudaStream_t stream);
+cudaError_t launch_plan(const kvc8_geom &g, const int32_t *context_lengths,
+                        const int64_t *context_seq_offset, int64_t *offsets_out, void *plan,
+                        int32_t *dev_error, cudaStream_t stream);
+// use_pdl: launch as a programmatic dependent of the previous kernel (the plan).
+cudaError_t launch_gather(const GatherArgs &a, bool use_pdl, cudaStream_t stream);
+
+// Per-device SM count (cached).
+int sm_count();
+
+}  // namespace kvc8

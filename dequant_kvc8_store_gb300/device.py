@@ -1,0 +1,118 @@
+"""Device-resident buffers for one store + gather problem, and the calls that
+run it through libkvc8.  Marshalling only: every step of the store and the
+gather runs in the library's kernels; torch allocates the memory and supplies
+the stream.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import binding as B
+from .workloads import Workload
+
+
+def _bf16(bits: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+
+
+def bf16_bits(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+class DeviceBatch:
+    """Holds a Workload on the GPU.
+
+    out_layout: "dense" -> outputs [rows][H][D];
+                "head_major" -> outputs stored [H][rows][D] and viewed as
+                [rows][H][D] (a transposed, strided view, as the pages' tests
+                pass with context_strided);
+    out_pad_rows: extra output rows after the last sequence (not written).
+    offsets: optional int64 [B] caller-given context_seq_offset.
+    """
+
+    def __init__(self, w: Workload, device="cuda", out_layout="dense", out_pad_rows=0,
+                 offsets=None, fill_out=None, pin=False):
+        self.w = w
+        self.device = torch.device(device)
+        dev = self.device
+        self.g = B.Geom(w.num_seqs, w.kv_heads, w.head_dim, w.block_size, w.num_blocks,
+                        w.max_blocks_per_seq, w.quant_mode)
+        H, D = w.kv_heads, w.head_dim
+        to = (lambda t: t.pin_memory()) if pin else (lambda t: t)
+        self.k_states = self.v_states = None
+        if w.has_store:
+            self.k_states = _bf16(w.k_states).to(dev)
+            self.v_states = _bf16(w.v_states).to(dev)
+        self.k_cache = torch.from_numpy(w.k_cache).to(dev)
+        self.v_cache = torch.from_numpy(w.v_cache).to(dev)
+        self.k_scale = torch.from_numpy(w.k_scale).to(dev)
+        self.v_scale = torch.from_numpy(w.v_scale).to(dev)
+        self.block_table = torch.from_numpy(w.block_table).to(dev)
+        self.cu_q_lens = None if w.cu_q_lens is None else torch.from_numpy(w.cu_q_lens).to(dev)
+        self.context_kv_lens = torch.from_numpy(w.context_kv_lens).to(dev)
+        self.context_lengths = torch.from_numpy(w.context_lengths).to(dev)
+        self.offsets = None
+        if offsets is not None:
+            self.offsets = torch.from_numpy(np.asarray(offsets, np.int64)).to(dev)
+            rows = int(max(int(o) + int(l) for o, l in zip(offsets, w.context_lengths))) if w.num_seqs else 0
+        else:
+            rows = w.total_context
+        self.out_rows = rows + out_pad_rows
+        if out_layout == "dense":
+            self.k_out = torch.empty((self.out_rows, H, D), dtype=torch.bfloat16, device=dev)
+            self.v_out = torch.empty((self.out_rows, H, D), dtype=torch.bfloat16, device=dev)
+        elif out_layout == "head_major":
+            self.k_out = torch.empty((H, self.out_rows, D), dtype=torch.bfloat16,
+                                     device=dev).transpose(0, 1)
+            self.v_out = torch.empty((H, self.out_rows, D), dtype=torch.bfloat16,
+                                     device=dev).transpose(0, 1)
+        else:
+            raise ValueError(out_layout)
+        if fill_out is not None:
+            self.k_out.view(torch.int16).fill_(np.int16(np.uint16(fill_out).view(np.int16)))
+            self.v_out.view(torch.int16).fill_(np.int16(np.uint16(fill_out).view(np.int16)))
+        self.ws_bytes = B.kvc8_gather_workspace_bytes(self.g)
+        self.workspace = torch.empty(max(self.ws_bytes, 256), dtype=torch.uint8, device=dev)
+        self.dev_error = torch.zeros(1, dtype=torch.int32, device=dev)
+        del to
+
+    # ---- the calls ------------------------------------------------------------
+
+    def store(self, stream=None):
+        if self.k_states is None:
+            return
+        ks = self.k_states
+        B.kvc8_store(self.g, ks.shape[0], ks, self.v_states, ks.stride(0), ks.stride(1),
+                     self.k_cache, self.v_cache, self.k_scale, self.v_scale, self.block_table,
+                     self.cu_q_lens, self.context_kv_lens, self.dev_error, stream)
+
+    def gather(self, stream=None):
+        ko = self.k_out
+        B.kvc8_dequant_gather(self.g, self.k_cache, self.v_cache, self.k_scale, self.v_scale,
+                              self.block_table, self.context_lengths, self.offsets, ko,
+                              self.v_out, self.out_rows, ko.stride(0), ko.stride(1),
+                              self.workspace, self.ws_bytes, self.dev_error, stream)
+
+    def build_metadata(self, offsets_out=None, stream=None):
+        B.kvc8_build_metadata(self.g, self.context_lengths, self.offsets, offsets_out,
+                              self.workspace, self.ws_bytes, self.dev_error, stream)
+
+    def gather_planned(self, stream=None):
+        ko = self.k_out
+        B.kvc8_dequant_gather_planned(self.g, self.k_cache, self.v_cache, self.k_scale,
+                                      self.v_scale, self.block_table, self.context_lengths, ko,
+                                      self.v_out, self.out_rows, ko.stride(0), ko.stride(1),
+                                      self.workspace, self.ws_bytes, self.dev_error, stream)
+
+    def error_code(self, reset=False) -> int:
+        return B.kvc8_get_error(self.dev_error, reset=reset)
+
+    # ---- host copies ------------------------------------------------------------
+
+    def host_caches(self):
+        return (self.k_cache.cpu().numpy(), self.v_cache.cpu().numpy(),
+                self.k_scale.cpu().numpy(), self.v_scale.cpu().numpy())
+
+    def host_outputs(self):
+        return bf16_bits(self.k_out), bf16_bits(self.v_out)

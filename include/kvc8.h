@@ -1,0 +1,246 @@
+/*
+ * kvc8.h -- C ABI of libkvc8: the int8 ("C8") paged KV-cache store and
+ * dequant-gather on NVIDIA GB300 (sm_103a).
+ *
+ * Source of the operations (web pages, cited by title and section):
+ *   [PR379]  mojo_opset pull request #379, "feat: [MLU] add mlu experimental
+ *            ops; fix post norm bug": the Gemini Code Assist review and the
+ *            four github-actions review passes, which describe the
+ *            torch-native MojoStorePagedKVCacheC8 and
+ *            MojoDequantFromPagedKVCache operators, their dequant_from_cache
+ *            helper, build_paged_kv_chunk_metadata and the context_seq_offset
+ *            default.
+ *   [README] "Mojo Opset" README, "Op List" (MojoStorePagedKVCache, the bf16
+ *            sibling) and "Backend Implementations / Torch native".
+ *
+ * Conventions shared by every entry point
+ *   - Every pointer argument is DEVICE memory on the CUDA device that is current
+ *     on the calling thread, unless the argument says "host".  The caller owns
+ *     all memory; the library allocates nothing and never synchronises the
+ *     stream (except kvc8_get_error, which exists to do so).
+ *   - Work is enqueued on `stream` and runs asynchronously.  Arguments that
+ *     can be checked on the host are checked before anything is enqueued; a
+ *     failed check returns KVC8_ERR_INVALID_ARG or KVC8_ERR_UNSUPPORTED and
+ *     enqueues nothing.
+ *   - Data-dependent errors (a block id outside the pool, a position beyond the
+ *     block table, an output row beyond out_rows, a negative length) can only be
+ *     seen on the device.  The kernels skip the offending row and record the
+ *     first such error in the optional device word `dev_error` (one int32_t,
+ *     0 = no error; the caller zeroes it).  They never trap.  Read it with
+ *     kvc8_get_error.
+ *   - Launch failures return KVC8_ERR_CUDA.
+ *
+ * Layouts (row-major, innermost last).  H = kv_heads, D = head_dim,
+ * bs = block_size, NB = num_blocks, B = num_seqs, MB = max_blocks_per_seq:
+ *   key_cache, value_cache   int8  [NB][H][bs][D]
+ *   scale cache (mode 0)     fp32  [NB][H][bs]     one scale per cached row
+ *   static scale (mode 1)    fp32  [H][D]          one scale per (head, channel)
+ *   block_table              int32 [B][MB]         physical block of each logical block
+ *   bf16 K/V tokens          [tokens][H][D] with element strides (tok_stride,
+ *                            head_stride, 1); both strides multiples of 8 and
+ *                            the base 16-byte aligned.
+ * The per-block layout [H][bs][D] follows from the review passes of [PR379]:
+ * the store writes key_cache[block, :, offset:offset+len, :] after permuting
+ * the new tokens to [heads, len, dim], the dequant helper broadcasts the scale
+ * with a token axis inserted before the channel axis, and the gather
+ * transposes [heads, tokens, dim] to [tokens, heads, dim].
+ *
+ * Arithmetic (bit-exact, no fast-math):
+ *   quantise     q = clamp(round_half_even(x / s), -127, 127), one IEEE fp32
+ *                division (q = 0 when s == 0)
+ *   mode 0 scale s = max_d |x_d| / 127 in fp32, per (token, kv head)
+ *   dequantise   out = bf16_round_nearest_even(fp32(q) * s), one fp32 multiply
+ */
+#ifndef KVC8_H
+#define KVC8_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum kvc8_status {
+    KVC8_OK = 0,
+    KVC8_ERR_INVALID_ARG = 1,   /* null pointer, bad size, stride or alignment */
+    KVC8_ERR_UNSUPPORTED = 2,   /* valid but outside what the kernels handle */
+    KVC8_ERR_CUDA = 3,          /* a CUDA call or launch failed */
+    KVC8_ERR_DEVICE_BOUNDS = 4, /* kvc8_get_error: the device word is set */
+    KVC8_ERR_WORKSPACE = 5      /* workspace missing, too small or misaligned */
+} kvc8_status;
+
+/* Codes the kernels write into the device error word (first error wins). */
+enum {
+    KVC8_DEV_OK = 0,
+    KVC8_DEV_BAD_BLOCK_ID = 1,     /* block_table entry outside [0, num_blocks) */
+    KVC8_DEV_POS_BEYOND_TABLE = 2, /* position >= max_blocks_per_seq * block_size */
+    KVC8_DEV_OUT_ROW_RANGE = 3,    /* gather output row outside [0, out_rows) */
+    KVC8_DEV_BAD_LENGTH = 4        /* negative length or decreasing cu_q_lens */
+};
+
+/* Geometry of one paged cache and one batch.  quant_mode: 0 = dynamic scale
+ * per (token, kv head), kept in a scale cache beside the codes; 1 = static
+ * scale per (kv head, channel), passed in.  [PR379] (every pass: the store is
+ * a symmetric int8 quantisation against a passed-in per-channel scale; the
+ * docstring says per_channal) describes the static form; the dynamic form
+ * stores its per-row scales where the pass-1 "Must fix" expects per-block
+ * scale shapes. */
+typedef struct kvc8_geom {
+    int32_t num_seqs;           /* B >= 0 */
+    int32_t kv_heads;           /* H >= 1 */
+    int32_t head_dim;           /* D: multiple of 16, 16..256 */
+    int32_t block_size;         /* bs >= 1 */
+    int32_t num_blocks;         /* NB >= 1 */
+    int32_t max_blocks_per_seq; /* MB >= 1 */
+    int32_t quant_mode;         /* 0 or 1 */
+} kvc8_geom;
+
+/* Human-readable name of a status code (static string). */
+const char *kvc8_status_str(kvc8_status status);
+
+/* Library version as major * 10000 + minor * 100 + patch. */
+int32_t kvc8_version(void);
+
+/*
+ * kvc8_store -- quantise new bf16 K and V tokens to int8 and scatter them into
+ * the paged cache: MojoStorePagedKVCacheC8 of [PR379].
+ *
+ * For sequence b (0 <= b < B) the new tokens are rows [cu_q_lens[b],
+ * cu_q_lens[b+1]) of key_states / value_states.  The i-th of them goes to
+ * logical position pos = context_kv_lens[b] + i, i.e. physical block
+ * block_table[b][pos / bs], slot pos % bs, for every kv head: the codes to
+ * cache[block][h][slot][0:D], and in mode 0 the row's scale to
+ * scale_cache[block][h][slot].  This replaces the pages' per-chunk host loop
+ * over build_paged_kv_chunk_metadata (pass-1 and pass-3 "Suggestions" on the
+ * Python loop and .tolist()) with per-token slot arithmetic on the device:
+ * one launch, no host synchronisation.
+ *
+ *   g              geometry (host pointer)
+ *   num_tokens     rows of key_states/value_states (N >= 0); 0 is a no-op
+ *   key_states,
+ *   value_states   bf16 [N][H][D], strides (x_tok_stride, x_head_stride, 1)
+ *                  in elements
+ *   key_cache,
+ *   value_cache    int8 [NB][H][bs][D], written in place
+ *   key_scale,
+ *   value_scale    mode 0: fp32 [NB][H][bs] scale caches, written in place;
+ *                  mode 1: fp32 [H][D] static scales, read only
+ *   block_table    int32 [B][MB]
+ *   cu_q_lens      int32 [B+1], cu_q_lens[0] = 0, non-decreasing, last = N;
+ *                  or NULL for pure decode: one new token per sequence, token
+ *                  b belongs to sequence b, and N must equal B (pass 2, "Must
+ *                  fix": cu_q_lens may be None in decode)
+ *   context_kv_lens int32 [B], tokens already cached per sequence
+ *   dev_error      optional int32 device word (see conventions), or NULL
+ *
+ * Tokens whose position leaves the block table or whose block id leaves the
+ * pool are skipped and reported through dev_error.  Sequences must not share
+ * physical blocks for the slots this call writes.
+ */
+kvc8_status kvc8_store(const kvc8_geom *g, int64_t num_tokens,
+                       const void *key_states, const void *value_states,
+                       int64_t x_tok_stride, int64_t x_head_stride,
+                       int8_t *key_cache, int8_t *value_cache,
+                       float *key_scale, float *value_scale,
+                       const int32_t *block_table, const int32_t *cu_q_lens,
+                       const int32_t *context_kv_lens, int32_t *dev_error,
+                       cudaStream_t stream);
+
+/* Bytes of device workspace that kvc8_build_metadata and kvc8_dequant_gather
+ * need for this geometry (depends on num_seqs only).  Host function. */
+size_t kvc8_gather_workspace_bytes(const kvc8_geom *g);
+
+/*
+ * kvc8_build_metadata -- the gather plan: per-sequence output offsets and the
+ * prefix of logical blocks per sequence, written into `workspace`.
+ *
+ * The output offsets are context_seq_offset when given, else the exclusive
+ * prefix sum of context_lengths: pass 1 and pass 3 ("Must fix" on
+ * context_seq_offset) describe the default as a cumsum shifted right by one
+ * with entry 0 = 0.  Computed on the device; no .item() and no host sync
+ * (pass-3 "Suggestions" on per-iteration .item()).
+ *
+ *   context_lengths     int32 [B], tokens to gather per sequence (>= 0)
+ *   context_seq_offset  int64 [B] caller-given first output row per sequence
+ *                       (padding between sequences allowed), or NULL
+ *   offsets_out         optional int64 [B]: receives the offsets used
+ *   workspace           >= kvc8_gather_workspace_bytes(g) bytes, 256-byte
+ *                       aligned; the plan stays valid while context_lengths,
+ *                       context_seq_offset and geometry are unchanged
+ */
+kvc8_status kvc8_build_metadata(const kvc8_geom *g, const int32_t *context_lengths,
+                                const int64_t *context_seq_offset,
+                                int64_t *offsets_out, void *workspace,
+                                size_t workspace_bytes, int32_t *dev_error,
+                                cudaStream_t stream);
+
+/*
+ * kvc8_dequant_gather -- gather every sequence's pages and dequantise them into
+ * contiguous bf16 rows: MojoDequantFromPagedKVCache of [PR379].
+ *
+ * For each b and p < context_lengths[b], for every kv head h and channel d:
+ *   out[(off_b + p) * out_tok_stride + h * out_head_stride + d]
+ *       = bf16(fp32(cache[blk][h][slot][d]) * s)
+ * with blk = block_table[b][p / bs], slot = p % bs, s = scale_cache[blk][h][slot]
+ * (mode 0) or static_scale[h][d] (mode 1), and off_b as in
+ * kvc8_build_metadata.  This is the pages' per-sequence loop (list-comprehension
+ * concat of the sequence's blocks, dequant_from_cache, slice to the context,
+ * transpose to [tokens, heads, dim], in-place write at the offset) as one
+ * pass with no host synchronisation.  Rows not covered by any sequence are not
+ * written.  The output may be strided (the pages' tests pass a transposed
+ * view); out_tok_stride and out_head_stride are in elements, multiples of 8,
+ * and key_out / value_out are 16-byte aligned.
+ *
+ * Enqueues the plan (kvc8_build_metadata into `workspace`) and the gather; the
+ * gather launch overlaps the plan's tail (programmatic dependent launch).
+ *
+ *   key_cache, value_cache   int8 [NB][H][bs][D]
+ *   key_scale, value_scale   mode 0: fp32 [NB][H][bs]; mode 1: fp32 [H][D]
+ *   block_table              int32 [B][MB]
+ *   context_lengths          int32 [B]
+ *   context_seq_offset       int64 [B] or NULL (exclusive prefix sum)
+ *   key_out, value_out       bf16, rows [0, out_rows)
+ *   workspace                as in kvc8_build_metadata
+ */
+kvc8_status kvc8_dequant_gather(const kvc8_geom *g, const int8_t *key_cache,
+                                const int8_t *value_cache, const float *key_scale,
+                                const float *value_scale, const int32_t *block_table,
+                                const int32_t *context_lengths,
+                                const int64_t *context_seq_offset, void *key_out,
+                                void *value_out, int64_t out_rows,
+                                int64_t out_tok_stride, int64_t out_head_stride,
+                                void *workspace, size_t workspace_bytes,
+                                int32_t *dev_error, cudaStream_t stream);
+
+/*
+ * kvc8_dequant_gather_planned -- kvc8_dequant_gather with a plan that an earlier
+ * kvc8_build_metadata wrote into `workspace` for the same context lengths,
+ * offsets and geometry (e.g. reused across the layers of one model step).
+ * One launch.  Arguments as in kvc8_dequant_gather.
+ */
+kvc8_status kvc8_dequant_gather_planned(const kvc8_geom *g, const int8_t *key_cache,
+                                        const int8_t *value_cache,
+                                        const float *key_scale, const float *value_scale,
+                                        const int32_t *block_table,
+                                        const int32_t *context_lengths, void *key_out,
+                                        void *value_out, int64_t out_rows,
+                                        int64_t out_tok_stride, int64_t out_head_stride,
+                                        const void *workspace, size_t workspace_bytes,
+                                        int32_t *dev_error, cudaStream_t stream);
+
+/*
+ * kvc8_get_error -- synchronise `stream`, copy the device error word to
+ * *host_code (host pointer) and return KVC8_ERR_DEVICE_BOUNDS if it is
+ * non-zero, KVC8_OK if zero.  With reset != 0 the word is zeroed afterwards.
+ */
+kvc8_status kvc8_get_error(int32_t *dev_error, int32_t *host_code, int32_t reset,
+                           cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVC8_H */
