@@ -102,7 +102,7 @@ SMALL = [
     dict(q_lens=[1] * 7, ctx_before=[0, 1, 15, 16, 17, 100, 63], kv_heads=8, head_dim=128,
          block_size=16, num_blocks=64, quant_mode=0, decode_null_cu=True),
     dict(q_lens=[300, 1, 1, 650], ctx_before=[0, 4000, 31, 700], kv_heads=8, head_dim=128,
-         block_size=64, num_blocks=120, quant_mode=1),
+         block_size=64, num_blocks=300, quant_mode=1),
     dict(q_lens=[129, 255, 1], ctx_before=[0, 1, 1023], kv_heads=8, head_dim=128,
          block_size=128, num_blocks=40, quant_mode=0, outlier_channels=4),
 ]
