@@ -11,7 +11,7 @@ per-token scales, N(0,1) K/V with 4 outlier channels per head (x20).  Other
 workloads: --workload tiny|decode|mixed|longctx.
 
 Timing: W untimed warm-up steps, then exactly K steps.  L2 is flushed (a
-256 MiB write) before each timed kernel; each op is bracketed by CUDA events on
+256 MiB write, then a 256 MiB read) before each timed kernel; each op is bracketed by CUDA events on
 the launching stream; the step time is the sum of its ops' event times.
 Barrier + synchronize on both sides; max over ranks.  SM clocks are sampled
 with nvidia-smi during the timed region.
