@@ -180,7 +180,7 @@ def run_gpu(args, rank, world):
         # write more than L2 holds, then read another buffer that size, so L2
         # ends up holding clean lines (no write-back competes with the next op)
         flush.fill_(v)
-        torch.sum(clean, out=sink)
+        torch.sum(clean, dim=0, out=sink)
     has_store = w.has_store and w.num_tokens > 0
 
     def barrier():
