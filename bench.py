@@ -188,7 +188,7 @@ def run_gpu(args, rank, world):
             torch.distributed.barrier()
         torch.cuda.synchronize()
 
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
 
     def step(e=None):
         flush_l2(1)
@@ -198,10 +198,8 @@ def run_gpu(args, rank, world):
         if e: e[1].record(stream)
         flush_l2(2)
         if e: e[2].record(stream)
-        d.build_metadata(stream=stream)
+        d.gather(stream)  # plan kernel + gather kernel (programmatic dependent launch)
         if e: e[3].record(stream)
-        d.gather_planned(stream)
-        if e: e[4].record(stream)
 
     for _ in range(args.warmup):
         step()
@@ -220,14 +218,12 @@ def run_gpu(args, rank, world):
         barrier()
         wall = time.perf_counter() - t0
     st_ms = [e[0].elapsed_time(e[1]) for e in ev]
-    plan_ms = [e[2].elapsed_time(e[3]) for e in ev]
-    ga_ms = [e[3].elapsed_time(e[4]) for e in ev]
-    step_ms = [a + b + c for a, b, c in zip(st_ms, plan_ms, ga_ms)]
+    ga_ms = [e[2].elapsed_time(e[3]) for e in ev]
+    step_ms = [a + b for a, b in zip(st_ms, ga_ms)]
     if d.error_code() != 0:
         raise RuntimeError("device error during the timed steps")
     local = {"step_ms": float(np.mean(step_ms)), "store_ms": float(np.mean(st_ms)),
-             "plan_ms": float(np.mean(plan_ms)), "gather_ms": float(np.mean(ga_ms)),
-             "wall_s": wall}
+             "gather_ms": float(np.mean(ga_ms)), "wall_s": wall}
     if world > 1:
         t = torch.tensor([local["step_ms"], local["store_ms"], local["gather_ms"]],
                          dtype=torch.float64, device=dev)
@@ -423,8 +419,7 @@ def main():
                       "GB_s": round(nbytes["store"] / (t["store_ms"] * 1e-3) / 1e9, 1) if has_store else None,
                       "tokens_per_s": round(w.num_tokens / (t["store_ms"] * 1e-3), 1) if has_store else None,
                       "bytes": nbytes["store"]},
-            "plan": {"ms": round(t["plan_ms"], 5)},
-            "dequant_gather": {"ms": round(t["gather_ms"], 5),
+            "dequant_gather": {"ms": round(t["gather_ms"], 5), "kernels": "plan + gather",
                                "GB_s": round(nbytes["gather"] / (t["gather_ms"] * 1e-3) / 1e9, 1),
                                "tokens_per_s": round(w.total_context / (t["gather_ms"] * 1e-3), 1),
                                "bytes": nbytes["gather"]},

@@ -100,8 +100,8 @@ kvc8_status kvc8_store(const kvc8_geom *g, int64_t num_tokens, const void *key_s
         return KVC8_ERR_INVALID_ARG;
     if (x_tok_stride < 0 || x_head_stride < 0 || x_tok_stride % 8 != 0 || x_head_stride % 8 != 0)
         return KVC8_ERR_INVALID_ARG;
-    if (!aligned(key_states, 16) || !aligned(value_states, 16) || !aligned(key_cache, 8) ||
-        !aligned(value_cache, 8))
+    if (!aligned(key_states, 16) || !aligned(value_states, 16) || !aligned(key_cache, 16) ||
+        !aligned(value_cache, 16))
         return KVC8_ERR_INVALID_ARG;
     if (!aligned(key_scale, 16) || !aligned(value_scale, 16)) return KVC8_ERR_INVALID_ARG;
     if (g->quant_mode == 1 && (int64_t)g->kv_heads * g->head_dim > kMaxStaticTable)
@@ -187,7 +187,7 @@ kvc8_status kvc8_dequant_gather_planned(const kvc8_geom *g, const int8_t *key_ca
                                         const int32_t *context_lengths, void *key_out,
                                         void *value_out, int64_t out_rows,
                                         int64_t out_tok_stride, int64_t out_head_stride,
-                                        const void *workspace, size_t workspace_bytes,
+                                        void *workspace, size_t workspace_bytes,
                                         int32_t *dev_error, cudaStream_t stream) {
     kvc8_status st = check_geom(g);
     if (st != KVC8_OK) return st;
@@ -213,6 +213,7 @@ kvc8_status kvc8_dequant_gather_planned(const kvc8_geom *g, const int8_t *key_ca
     a.out_head_stride = out_head_stride;
     a.plan = workspace;
     a.dev_error = dev_error;
+    if (reset_plan_counter(workspace, stream) != cudaSuccess) return KVC8_ERR_CUDA;
     return cuda_status(launch_gather(a, /*use_pdl=*/false, stream));
 }
 

@@ -4,17 +4,19 @@
 // plan kernel that replaces the pages' host-side offset cumsum and per-batch
 // .item() loop.
 //
-// Work decomposition.  A tile is one logical block j of one sequence b; a unit
+// Work decomposition.  A tile is one logical block j of one sequence b; a slab
 // is one (tile, K|V, kv head): bs rows of D int8 codes, contiguous in the
 // cache ([blk][h][0:bs][0:D]), that land as bs rows of D bf16 values at
 // out[(off_b + j*bs + slot)][h][:] -- a 2*D-byte contiguous segment per row.
-// Units are numbered tile-major and dealt round-robin to a persistent grid, so
-// every CTA streams equal-sized units regardless of how ragged the sequence
-// lengths are.  Inside a unit each thread moves 16-byte chunks (16 codes ->
-// 32 bytes of bf16), four chunks in flight per thread.  Source reads and
-// destination writes are both fully coalesced without a shared-memory
-// transpose, because the transpose [heads, tokens, dim] -> [tokens, heads, dim]
-// only permutes whole D-element rows.
+// A work item is a tile and a pair of its slabs; items are numbered tile-major
+// and handed to a persistent grid through an atomic counter, so every CTA keeps
+// streaming equal-sized items however ragged the sequence lengths are.  Inside
+// an item each thread moves chunks of 32 codes (256-bit loads; 16 when D is not
+// a multiple of 32) -> 64 bytes of bf16, two chunks per slab, so four loads
+// (128 bytes) are in flight per thread.  Source reads and destination writes
+// are both fully coalesced without a shared-memory transpose, because the
+// transpose [heads, tokens, dim] -> [tokens, heads, dim] only permutes whole
+// D-element rows.
 //
 // Arithmetic per element: c = int8 code, exactly recovered as float by the
 // bias trick (0x4B000000 | (c + 128)) - (2^23 + 128); v = c * s in one IEEE
@@ -26,7 +28,6 @@ namespace {
 
 constexpr int kPlanThreads = 1024;
 constexpr int kGatherThreads = 256;
-constexpr int kUnroll = 4;
 
 // ---------------------------------------------------------------------------
 // Plan: one CTA scans context_lengths (int64 running sum for the offsets and an
@@ -112,7 +113,9 @@ plan_kernel(const kvc8_geom g, const int32_t *__restrict__ lens,
     }
     if (threadIdx.x == 0) {
         ts[B] = carry_tiles_s;
-        reinterpret_cast<PlanHeader *>(plan)->total_tiles = carry_tiles_s;
+        PlanHeader *hdr = reinterpret_cast<PlanHeader *>(plan);
+        hdr->total_tiles = carry_tiles_s;
+        hdr->work_counter = 0;  // the gather's work distribution starts afresh
     }
 }
 
@@ -129,7 +132,7 @@ __device__ __forceinline__ int seq_of_tile(const int32_t *ts, int B, int64_t til
     return lo;
 }
 
-// Four int8 codes -> four exact floats.
+// Four int8 codes -> four exact floats: (0x4B000000 | (c + 128)) - (2^23 + 128).
 __device__ __forceinline__ void codes_to_f32(uint32_t w, float f[4]) {
     const uint32_t wb = w ^ 0x80808080u;  // c + 128 per byte
     const float bias = 8388736.0f;        // 2^23 + 128
@@ -145,143 +148,189 @@ __device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
     return r;
 }
 
-// 16 codes with one scale each (sc[e] for element e) -> 8 packed bf16 pairs.
-__device__ __forceinline__ void dequant16(const uint4 v, const float *sc, uint32_t out[8]) {
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+// One chunk of CH codes (CH/4 words) -> CH/2 packed bf16 pairs.  Mode 0: one
+// scale for the chunk; mode 1: per-channel scales sc[0..CH).
+template <int CH, int MODE>
+__device__ __forceinline__ void dequant_chunk(const uint32_t *w, float s, const float *sc,
+                                              uint32_t *o) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < CH / 4; ++j) {
         float f[4];
         codes_to_f32(w[j], f);
-        const float p0 = __fmul_rn(f[0], sc[4 * j + 0]);
-        const float p1 = __fmul_rn(f[1], sc[4 * j + 1]);
-        const float p2 = __fmul_rn(f[2], sc[4 * j + 2]);
-        const float p3 = __fmul_rn(f[3], sc[4 * j + 3]);
-        out[2 * j] = bf16x2_rn(p0, p1);
-        out[2 * j + 1] = bf16x2_rn(p2, p3);
+        float p[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) p[e] = __fmul_rn(f[e], MODE == 0 ? s : sc[4 * j + e]);
+        o[2 * j] = bf16x2_rn(p[0], p[1]);
+        o[2 * j + 1] = bf16x2_rn(p[2], p[3]);
     }
 }
 
-template <int MODE, bool WIDE>
+template <int CH>
+__device__ __forceinline__ void load_chunk(const int8_t *p, uint32_t *w) {
+    if (CH == 32) {
+        asm("ld.global.nc.L1::no_allocate.v8.u32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+            : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]),
+              "=r"(w[6]), "=r"(w[7])
+            : "l"(p));
+    } else {
+        const uint4 v = ld_stream_16(p);
+        w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+    }
+}
+
+template <int CH, bool WIDE>
+__device__ __forceinline__ void store_chunk(uint16_t *p, const uint32_t *o) {
+#pragma unroll
+    for (int q = 0; q < CH / 16; ++q) {
+        if (WIDE) {
+            st_stream_32(p + 16 * q, make_uint4(o[8 * q], o[8 * q + 1], o[8 * q + 2], o[8 * q + 3]),
+                         make_uint4(o[8 * q + 4], o[8 * q + 5], o[8 * q + 6], o[8 * q + 7]));
+        } else {
+            st_stream_16(p + 16 * q, o[8 * q], o[8 * q + 1], o[8 * q + 2], o[8 * q + 3]);
+            st_stream_16(p + 16 * q + 8, o[8 * q + 4], o[8 * q + 5], o[8 * q + 6], o[8 * q + 7]);
+        }
+    }
+}
+
+// A work item is one tile (sequence b, logical block j) and a pair of (K|V,
+// head) slabs: units 2r and 2r+1 of the tile's 2H units, so both slabs share
+// the tile's metadata.  Items are handed out by an atomic counter in the plan.
+template <int MODE, int CH, bool WIDE>
 __global__ void __launch_bounds__(kGatherThreads)
 gather_kernel(const GatherArgs a) {
+    constexpr int W = CH / 4;  // words per chunk
+    constexpr int PER = 2;     // chunks per slab per thread per round
     const int H = a.g.kv_heads, D = a.g.head_dim, bs = a.g.block_size;
     const int B = a.g.num_seqs, MB = a.g.max_blocks_per_seq, NB = a.g.num_blocks;
-    const int CPR = D >> 4;  // 16-code chunks per row
-    const bool col_fixed = (kGatherThreads % CPR) == 0;
+    const int CPR = D / CH;  // chunks per row
 
-    pdl_wait_prior_grid();
+    extern __shared__ float s_tab[];  // mode 1: static scales [2][H][D]
+    if (MODE == 1) {
+        for (int i = threadIdx.x; i < 2 * H * D; i += blockDim.x)
+            s_tab[i] = i < H * D ? ld_nc_f32(a.k_scale + i) : ld_nc_f32(a.v_scale + (i - H * D));
+        __syncthreads();
+    }
+    __shared__ long long s_item;
+
+    pdl_wait_prior_grid();  // the plan (and its counter reset) is complete
     const char *plan = static_cast<const char *>(a.plan);
+    const PlanHeader *hdr = reinterpret_cast<const PlanHeader *>(plan);
     const int64_t *off = reinterpret_cast<const int64_t *>(plan + plan_offsets_at(B));
     const int32_t *ts = reinterpret_cast<const int32_t *>(plan + plan_tile_start_at(B));
-    const int64_t total_tiles = reinterpret_cast<const PlanHeader *>(plan)->total_tiles;
-    const int64_t units = total_tiles * 2 * H;
+    unsigned long long *counter =
+        reinterpret_cast<unsigned long long *>(const_cast<int64_t *>(&hdr->work_counter));
+    const int64_t items = hdr->total_tiles * H;
 
-    for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
-        const int64_t tile = u / (2 * H);
-        const int r = (int)(u - tile * 2 * H);
-        const int kv = r >= H;
-        const int h = r - kv * H;
+    int64_t item = blockIdx.x;
+    while (item < items) {
+        long long next = 0;
+        if (threadIdx.x == 0) next = (long long)atomicAdd(counter, 1ull) + gridDim.x;
+
+        const int64_t tile = item / H;
+        const int r2 = (int)(item - tile * H);
         const int b = seq_of_tile(ts, B, tile);
         const int64_t j = tile - ts[b];
-        int64_t len = ld_nc_s32(a.context_lengths + b);
+        const int64_t len = ld_nc_s32(a.context_lengths + b);
         const int nvalid = (int)min((int64_t)bs, len - j * bs);
         const int32_t blk = ld_nc_s32(a.block_table + (int64_t)b * MB + j);
         const int64_t row0 = off[b] + j * bs;
+        bool ok = true;
         if (blk < 0 || blk >= NB) {
             if (threadIdx.x == 0) report(a.dev_error, KVC8_DEV_BAD_BLOCK_ID);
-            continue;
-        }
-        if (row0 < 0 || row0 + nvalid > a.out_rows) {
+            ok = false;
+        } else if (row0 < 0 || row0 + nvalid > a.out_rows) {
             if (threadIdx.x == 0) report(a.dev_error, KVC8_DEV_OUT_ROW_RANGE);
-            continue;
+            ok = false;
         }
-        const int8_t *src = (kv ? a.v_cache : a.k_cache) + ((int64_t)blk * H + h) * bs * D;
-        const float *scl = kv ? a.v_scale : a.k_scale;
-        uint16_t *dst = (kv ? a.v_out : a.k_out) + row0 * a.out_tok_stride +
-                        (int64_t)h * a.out_head_stride;
-        const float *row_scale = scl + ((int64_t)blk * H + h) * bs;  // mode 0
-        const float *chan_scale = scl + (int64_t)h * D;               // mode 1
-
-        float fixed_sc[16];
-        if (MODE == 1 && col_fixed) {
-            const int col = threadIdx.x % CPR;
+        if (ok) {
+            const int8_t *src[2];
+            const float *rsc[2];
+            const float *csc[2];
+            uint16_t *dst[2];
 #pragma unroll
-            for (int e = 0; e < 16; e += 4) {
-                const float4 s4 = __ldg(reinterpret_cast<const float4 *>(chan_scale + col * 16 + e));
-                fixed_sc[e] = s4.x; fixed_sc[e + 1] = s4.y; fixed_sc[e + 2] = s4.z; fixed_sc[e + 3] = s4.w;
+            for (int sl = 0; sl < 2; ++sl) {
+                const int u = 2 * r2 + sl;
+                const int kv = u >= H;
+                const int h = u - kv * H;
+                src[sl] = (kv ? a.v_cache : a.k_cache) + ((int64_t)blk * H + h) * bs * D;
+                rsc[sl] = (kv ? a.v_scale : a.k_scale) + ((int64_t)blk * H + h) * bs;
+                csc[sl] = s_tab + (kv * H + h) * D;
+                dst[sl] = (kv ? a.v_out : a.k_out) + row0 * a.out_tok_stride +
+                          (int64_t)h * a.out_head_stride;
             }
-        }
-
-        const int nchunks = nvalid * CPR;
-        for (int c0 = 0; c0 < nchunks; c0 += kGatherThreads * kUnroll) {
-            uint4 v[kUnroll];
-            float s[kUnroll];
+            const int nch = nvalid * CPR;  // chunks per slab
+            for (int c0 = 0; c0 < nch; c0 += kGatherThreads * PER) {
+                uint32_t w[2][PER][W];
+                float s[2][PER];
 #pragma unroll
-            for (int k = 0; k < kUnroll; ++k) {
-                const int c = c0 + k * kGatherThreads + threadIdx.x;
-                v[k] = make_uint4(0u, 0u, 0u, 0u);
-                s[k] = 0.0f;
-                if (c < nchunks) {
-                    v[k] = ld_stream_16(src + (int64_t)c * 16);
-                    if (MODE == 0) s[k] = ld_nc_f32(row_scale + c / CPR);
-                }
-            }
+                for (int sl = 0; sl < 2; ++sl) {
 #pragma unroll
-            for (int k = 0; k < kUnroll; ++k) {
-                const int c = c0 + k * kGatherThreads + threadIdx.x;
-                if (c >= nchunks) continue;
-                const int row = c / CPR;
-                const int col = c - row * CPR;
-                float sc[16];
-                if (MODE == 0) {
+                    for (int k = 0; k < PER; ++k) {
+                        const int c = c0 + k * kGatherThreads + threadIdx.x;
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) sc[e] = s[k];
-                } else if (col_fixed) {
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) sc[e] = fixed_sc[e];
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 16; e += 4) {
-                        const float4 s4 = __ldg(reinterpret_cast<const float4 *>(chan_scale + col * 16 + e));
-                        sc[e] = s4.x; sc[e + 1] = s4.y; sc[e + 2] = s4.z; sc[e + 3] = s4.w;
+                        for (int i = 0; i < W; ++i) w[sl][k][i] = 0u;
+                        s[sl][k] = 0.0f;
+                        if (c < nch) {
+                            load_chunk<CH>(src[sl] + (int64_t)c * CH, w[sl][k]);
+                            if (MODE == 0) s[sl][k] = ld_nc_f32(rsc[sl] + c / CPR);
+                        }
                     }
                 }
-                uint32_t o[8];
-                dequant16(v[k], sc, o);
-                uint16_t *p = dst + (int64_t)row * a.out_tok_stride + col * 16;
-                if (WIDE) {
-                    st_stream_32(p, make_uint4(o[0], o[1], o[2], o[3]), make_uint4(o[4], o[5], o[6], o[7]));
-                } else {
-                    st_stream_16(p, o[0], o[1], o[2], o[3]);
-                    st_stream_16(p + 8, o[4], o[5], o[6], o[7]);
+#pragma unroll
+                for (int sl = 0; sl < 2; ++sl) {
+#pragma unroll
+                    for (int k = 0; k < PER; ++k) {
+                        const int c = c0 + k * kGatherThreads + threadIdx.x;
+                        if (c >= nch) continue;
+                        const int row = c / CPR;
+                        const int col = c - row * CPR;
+                        uint32_t o[CH / 2];
+                        dequant_chunk<CH, MODE>(w[sl][k], s[sl][k], csc[sl] + col * CH, o);
+                        store_chunk<CH, WIDE>(dst[sl] + (int64_t)row * a.out_tok_stride + col * CH, o);
+                    }
                 }
             }
         }
+        if (threadIdx.x == 0) s_item = next;
+        __syncthreads();
+        item = s_item;
+        __syncthreads();
     }
 }
 
-template <int MODE, bool WIDE>
+template <int MODE, int CH, bool WIDE>
 cudaError_t launch_gather_variant(const GatherArgs &a, bool use_pdl, cudaStream_t stream) {
-    auto kern = gather_kernel<MODE, WIDE>;
-    static int occ_cached[64];
+    auto kern = gather_kernel<MODE, CH, WIDE>;
+    const size_t smem = MODE == 1 ? sizeof(float) * 2 * a.g.kv_heads * a.g.head_dim : 0;
+    static int cached_dev = -1;
+    static size_t cached_smem = 0;
+    static int cached_occ = 0;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    int occ = dev < 64 ? occ_cached[dev] : 0;
-    if (occ == 0) {
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kGatherThreads, 0);
+    if (smem > 48 * 1024) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    int occ = 0;
+    if (cached_dev == dev && cached_smem == smem) {
+        occ = cached_occ;
+    } else {
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kGatherThreads, smem);
         if (e != cudaSuccess) return e;
         if (occ < 1) occ = 1;
-        if (dev < 64) occ_cached[dev] = occ;
+        cached_occ = occ;
+        cached_smem = smem;
+        cached_dev = dev;
     }
-    const int64_t max_units = (int64_t)a.g.num_seqs * a.g.max_blocks_per_seq * 2 * a.g.kv_heads;
+    const int64_t max_items = (int64_t)a.g.num_seqs * a.g.max_blocks_per_seq * a.g.kv_heads;
     const int64_t cap = (int64_t)sm_count() * occ;
-    const int grid = (int)(max_units < cap ? max_units : cap);
+    const int grid = (int)(max_items < cap ? max_items : cap);
     if (grid <= 0) return cudaSuccess;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kGatherThreads);
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -289,6 +338,12 @@ cudaError_t launch_gather_variant(const GatherArgs &a, bool use_pdl, cudaStream_
     cfg.attrs = attr;
     cfg.numAttrs = use_pdl ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
+template <int MODE, bool WIDE>
+cudaError_t launch_gather_mode(const GatherArgs &a, bool use_pdl, cudaStream_t stream) {
+    if (a.g.head_dim % 32 == 0) return launch_gather_variant<MODE, 32, WIDE>(a, use_pdl, stream);
+    return launch_gather_variant<MODE, 16, WIDE>(a, use_pdl, stream);
 }
 
 }  // namespace
@@ -301,16 +356,21 @@ cudaError_t launch_plan(const kvc8_geom &g, const int32_t *context_lengths,
     return cudaGetLastError();
 }
 
+cudaError_t reset_plan_counter(void *plan, cudaStream_t stream) {
+    return cudaMemsetAsync(static_cast<char *>(plan) + offsetof(PlanHeader, work_counter), 0,
+                           sizeof(int64_t), stream);
+}
+
 cudaError_t launch_gather(const GatherArgs &a, bool use_pdl, cudaStream_t stream) {
     const uintptr_t k = reinterpret_cast<uintptr_t>(a.k_out);
     const uintptr_t v = reinterpret_cast<uintptr_t>(a.v_out);
     const bool wide = (k % 32 == 0) && (v % 32 == 0) && (a.out_tok_stride % 16 == 0) &&
                       (a.out_head_stride % 16 == 0);
     if (a.g.quant_mode == 0)
-        return wide ? launch_gather_variant<0, true>(a, use_pdl, stream)
-                    : launch_gather_variant<0, false>(a, use_pdl, stream);
-    return wide ? launch_gather_variant<1, true>(a, use_pdl, stream)
-                : launch_gather_variant<1, false>(a, use_pdl, stream);
+        return wide ? launch_gather_mode<0, true>(a, use_pdl, stream)
+                    : launch_gather_mode<0, false>(a, use_pdl, stream);
+    return wide ? launch_gather_mode<1, true>(a, use_pdl, stream)
+                : launch_gather_mode<1, false>(a, use_pdl, stream);
 }
 
 }  // namespace kvc8

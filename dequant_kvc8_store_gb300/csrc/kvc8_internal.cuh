@@ -75,11 +75,13 @@ __device__ __forceinline__ void report(int32_t *dev_error, int32_t code) {
 // ---------------------------------------------------------------------------
 // Gather plan, written by the plan kernel into the caller's workspace.
 //   header.total_tiles : number of (sequence, logical block) tiles
+//   header.work_counter: next work item of the gather (reset by the plan)
 //   offsets[B]         : first output row of each sequence (int64)
 //   tile_start[B + 1]  : exclusive prefix of ceil(len_b / bs), tile_start[B] = total
 struct PlanHeader {
     int64_t total_tiles;
-    int64_t pad[3];
+    int64_t work_counter;  // gather work items handed out so far (atomic)
+    int64_t pad[2];
 };
 
 constexpr size_t kAlign = 256;
@@ -137,6 +139,8 @@ cudaError_t launch_plan(const kvc8_geom &g, const int32_t *context_lengths,
                         int32_t *dev_error, cudaStream_t stream);
 // use_pdl: launch as a programmatic dependent of the previous kernel (the plan).
 cudaError_t launch_gather(const GatherArgs &a, bool use_pdl, cudaStream_t stream);
+// Zero the gather's work counter in a plan built earlier (for planned gathers).
+cudaError_t reset_plan_counter(void *plan, cudaStream_t stream);
 
 // Per-device SM count (cached).
 int sm_count();

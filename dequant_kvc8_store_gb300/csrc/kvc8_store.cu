@@ -3,29 +3,65 @@
 // "feat: [MLU] add mlu experimental ops; fix post norm bug").
 //
 // Work decomposition: one warp per token.  A token carries 2*H rows (K heads,
-// then V heads) of D bf16 values.  A row is split into D/8 chunks of 16 bytes,
-// one chunk per lane, so a pass of the warp covers 32/LANES rows; all passes of
-// a token (up to 8) are loaded before any is converted, so every lane keeps up
-// to 128 bytes of loads in flight.  The grid is persistent (a multiple of the
-// SM count) and warps stride over tokens.
+// then V heads) of D bf16 values.  Each lane owns E consecutive values of a row
+// (E = 32 when D is a multiple of 32, else 16), so LANES = D/E lanes (rounded
+// up to a power of two) cover a row and a warp pass covers 32/LANES rows.  The
+// row data of a token is requested before its slot is computed, so the
+// metadata lookups overlap the loads.  The grid is persistent (a multiple of
+// the SM count) and warps stride over tokens.
 //
 // Rounding is bit-exact with the definition q = clamp(rne(x / s), -127, 127)
-// (one IEEE fp32 division).  Per element the kernel first evaluates
-// y = x * fl(1/s); the relative error of y against the exact quotient t = x/s
-// is at most 2^-23 + 2^-48, i.e. below 2^-15 for |t| <= 256.  Where y is more
-// than 2^-13 away from every half-integer, t and fl(t) lie strictly inside the
-// same interval between half-integers as y, so rne(y) = rne(fl(t)) and the
-// fast path is exact.  Inside that window (and for scales whose reciprocal
-// could leave the normal range) the element is recomputed with the IEEE
-// division __fdiv_rn and __float2int_rn.  Values with |y| > 200 saturate
-// (then |t| > 199.99 and the code is +-127 either way).
+// (one IEEE fp32 division).  Per element the kernel evaluates y = x * r with
+// r = fl(1/s) (correctly rounded), in packed fp32x2 arithmetic.  The relative
+// error of y against the exact quotient t = x/s is at most 2^-23 + 2^-48, so
+// |y - t| < 1.55e-5 whenever |t| <= 130; fl(t) is within half an ulp of t
+// (<= 7.7e-6 below 256).  If y lies more than 2^-15 (3.05e-5) from every
+// half-integer, then t and fl(t) lie strictly inside the same interval between
+// half-integers as y, and rne(y) = rne(fl(t)).  y is rounded by adding
+// 1.5 * 2^23 (RNE to an integer, whose low byte is the code).  A lane whose
+// values come within 2^-15 of a half-integer (about 0.2% of 32-value lanes)
+// recomputes those values with __fdiv_rn + __float2int_rn.  In static mode y
+// is first clamped to [-127, 127]: |y| >= 127 means |t| >= 126.99998, whose
+// code is +-127 on both paths, and values below are untouched (in dynamic mode
+// |y| <= 127.00003 already).  Scales whose
+// reciprocal could leave the normal range (and zero scales) always take the
+// exact path.
 #include "kvc8_internal.cuh"
 
 namespace kvc8 {
 namespace {
 
 constexpr int kWarpsPerCta = 8;
-constexpr int kGroup = 8;  // row passes loaded before converting
+constexpr float kMagic = 12582912.0f;            // 1.5 * 2^23
+constexpr float kNearTie = 0.499969482421875f;   // 0.5 - 2^-15
+constexpr float kSatClamp = 127.0f;   // |y| >= 127 gives +-127 on both paths
+
+typedef unsigned long long u64;
+
+__device__ __forceinline__ u64 pk(float lo, float hi) {
+    u64 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void upk(u64 v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ u64 mul2(u64 a, u64 b) {
+    u64 r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ u64 add2(u64 a, u64 b) {
+    u64 r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+// a * b + c, one rounding per lane
+__device__ __forceinline__ u64 fma2(u64 a, u64 b, u64 c) {
+    u64 r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
 
 // Reciprocal fast path needs s and 1/s normal and finite.
 __device__ __forceinline__ bool recip_ok(float s) {
@@ -39,28 +75,20 @@ __device__ __noinline__ int quant_exact(float x, float s) {
     return min(127, max(-127, q));
 }
 
-// Fast path: returns the code of y = x * r and sets `near` when y is within
-// 2^-13 of a half-integer (the exact path must decide).
-__device__ __forceinline__ int quant_fast(float x, float r, bool &near) {
-    const float kMagic = 12582912.0f;  // 1.5 * 2^23: adding it rounds to an integer (RNE)
-    float y = __fmul_rn(x, r);
-    y = fminf(fmaxf(y, -200.0f), 200.0f);
+// Code of one value on the fast path (r != 0), or the exact path when the
+// value is near a tie, r == 0 marks an out-of-range scale, or force is set.
+__device__ __forceinline__ int quant_one(float x, float s, float r) {
+    if (r == 0.0f) return quant_exact(x, s);
+    float y = fminf(fmaxf(__fmul_rn(x, r), -kSatClamp), kSatClamp);
     float m = __fadd_rn(y, kMagic);
-    float k = __fsub_rn(m, kMagic);
-    float d = __fsub_rn(y, k);
-    near = fabsf(d) >= 0.4998779296875f;  // 0.5 - 2^-13
-    int q = __float_as_int(m) - 0x4B400000;
-    return min(127, max(-127, q));
+    float d = __fsub_rn(y, __fsub_rn(m, kMagic));
+    if (fabsf(d) >= kNearTie) return quant_exact(x, s);
+    return __float_as_int(m) - 0x4B400000;
 }
 
-__device__ __forceinline__ uint32_t pack4(int q0, int q1, int q2, int q3) {
-    uint32_t t01 = __byte_perm((uint32_t)q0, (uint32_t)q1, 0x0040);
-    uint32_t t23 = __byte_perm((uint32_t)q2, (uint32_t)q3, 0x0040);
-    return __byte_perm(t01, t23, 0x5410);
+__device__ __forceinline__ uint32_t pack_lo_bytes(uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    return __byte_perm(__byte_perm(a, b, 0x0040), __byte_perm(c, d, 0x0040), 0x5410);
 }
-
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
 // Largest b in [0, B] with cu[b] <= t (cu[0] = 0 <= t).
 __device__ __forceinline__ int seq_of_token(const int32_t *cu, int B, int64_t t) {
@@ -72,153 +100,222 @@ __device__ __forceinline__ int seq_of_token(const int32_t *cu, int B, int64_t t)
     return lo;
 }
 
-template <int LANES, int MODE>
-__global__ void __launch_bounds__(kWarpsPerCta * 32)
+template <bool V32>
+__device__ __forceinline__ void load32(const uint16_t *p, uint32_t w[8]) {
+    if (V32) {
+        asm("ld.global.nc.L1::no_allocate.v8.u32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+            : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]),
+              "=r"(w[6]), "=r"(w[7])
+            : "l"(p));
+    } else {
+        const uint4 a = ld_stream_16(p), b = ld_stream_16(p + 8);
+        w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+        w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+    }
+}
+
+template <bool V32>
+__device__ __forceinline__ void store_codes32(int8_t *p, const uint32_t c[8]) {
+    if (V32) {
+        asm volatile("st.global.v8.u32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p),
+                     "r"(c[0]), "r"(c[1]), "r"(c[2]), "r"(c[3]), "r"(c[4]), "r"(c[5]), "r"(c[6]),
+                     "r"(c[7])
+                     : "memory");
+    } else {
+        asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(c[0]), "r"(c[1]),
+                     "r"(c[2]), "r"(c[3])
+                     : "memory");
+        asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p + 16), "r"(c[4]),
+                     "r"(c[5]), "r"(c[6]), "r"(c[7])
+                     : "memory");
+    }
+}
+
+__device__ __forceinline__ void store_codes16(int8_t *p, const uint32_t c[4]) {
+    asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(c[0]), "r"(c[1]),
+                 "r"(c[2]), "r"(c[3])
+                 : "memory");
+}
+
+// E values per lane (16 or 32), LANES lanes per row, MODE 0 dynamic / 1 static,
+// V32: 32-byte aligned rows (256-bit loads and stores).
+template <int E, int LANES, int MODE, bool V32>
+__global__ void __launch_bounds__(kWarpsPerCta * 32, 3)
 store_kernel(const StoreArgs a) {
-    constexpr int RPP = 32 / LANES;  // rows per warp pass
+    constexpr int W = E / 2;                  // bf16x2 words per lane per row
+    constexpr int RPP = 32 / LANES;           // rows per warp pass
+    constexpr int G = (E == 32) ? 2 : 4;      // passes loaded ahead
     const int H = a.g.kv_heads, D = a.g.head_dim, bs = a.g.block_size;
     const int B = a.g.num_seqs, MB = a.g.max_blocks_per_seq, NB = a.g.num_blocks;
-    const int C = D >> 3;  // 16-byte chunks per row
+    const int C = D / E;  // active lanes per row
     const int lane = threadIdx.x & 31;
     const int sub = lane / LANES;
     const int c = lane % LANES;
     const bool lane_on = c < C;
 
-    // Static mode: per-(kv, head, channel) scale and reciprocal tables in shared
-    // memory, [2][H][D] each; a zero reciprocal marks "use the exact path".
+    // Static mode: scale and reciprocal tables [2][H][D] in shared memory; a
+    // zero reciprocal marks a scale that must take the exact path.
     extern __shared__ float smem[];
     float *s_tab = smem;
     float *r_tab = smem + 2 * H * D;
+    bool all_fast = true;
     if (MODE == 1) {
+        int ok = 1;
         for (int i = threadIdx.x; i < 2 * H * D; i += blockDim.x) {
             float s = i < H * D ? ld_nc_f32(a.k_scale + i) : ld_nc_f32(a.v_scale + (i - H * D));
             s_tab[i] = s;
-            r_tab[i] = recip_ok(s) ? __frcp_rn(s) : 0.0f;
+            const bool f = recip_ok(s);
+            r_tab[i] = f ? __frcp_rn(s) : 0.0f;
+            ok &= f;
         }
-        __syncthreads();
+        all_fast = __syncthreads_and(ok) != 0;
     }
 
     const int rows = 2 * H;
     const int passes = (rows + RPP - 1) / RPP;
     const int64_t nwarps = (int64_t)gridDim.x * kWarpsPerCta;
+    const u64 magic2 = pk(kMagic, kMagic);
+    const u64 nmagic2 = pk(-kMagic, -kMagic);
+    const u64 neg1 = pk(-1.0f, -1.0f);
+
     for (int64_t t = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5); t < a.num_tokens;
          t += nwarps) {
-        // ---- slot of token t (warp-uniform) ----
-        int b;
-        int64_t i_in_seq;
-        bool bad_len = false;
-        if (a.cu_q_lens != nullptr) {
-            b = seq_of_token(a.cu_q_lens, B, t);
-            int64_t first = ld_nc_s32(a.cu_q_lens + b);
-            int64_t next = ld_nc_s32(a.cu_q_lens + b + 1);
-            i_in_seq = t - first;
-            bad_len = !(first <= t && t < next);
-        } else {
-            b = (int)t;
-            i_in_seq = 0;
-        }
-        int64_t ctx = ld_nc_s32(a.context_kv_lens + b);
-        int64_t pos = ctx + i_in_seq;
-        int64_t lb = pos / bs;
-        int32_t err = 0;
-        int32_t blk = 0;
-        if (bad_len || ctx < 0) {
-            err = KVC8_DEV_BAD_LENGTH;
-        } else if (lb >= MB) {
-            err = KVC8_DEV_POS_BEYOND_TABLE;
-        } else {
-            blk = ld_nc_s32(a.block_table + (int64_t)b * MB + lb);
-            if (blk < 0 || blk >= NB) err = KVC8_DEV_BAD_BLOCK_ID;
-        }
-        if (err != 0) {
-            if (lane == 0) report(a.dev_error, err);
-            continue;
-        }
-        const int64_t slot = pos - lb * bs;
-
-        for (int p0 = 0; p0 < passes; p0 += kGroup) {
-            uint4 v[kGroup];
+        for (int p0 = 0; p0 < passes; p0 += G) {
+            // ---- request this group's rows ----
+            uint32_t w[G][W];
 #pragma unroll
-            for (int k = 0; k < kGroup; ++k) {
+            for (int k = 0; k < G; ++k) {
                 const int row = (p0 + k) * RPP + sub;
-                v[k] = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                for (int i = 0; i < W; ++i) w[k][i] = 0u;
                 if (p0 + k < passes && row < rows && lane_on) {
                     const int kv = row >= H;
                     const int h = row - kv * H;
                     const uint16_t *src = (kv ? a.v_states : a.k_states) + t * a.x_tok_stride +
-                                          (int64_t)h * a.x_head_stride + c * 8;
-                    v[k] = ld_stream_16(src);
+                                          (int64_t)h * a.x_head_stride + c * E;
+                    load32<V32>(src, w[k]);
+                    if (E == 32) load32<V32>(src + 16, w[k] + 8);
                 }
             }
+            // ---- slot of token t (warp-uniform), overlapping the loads ----
+            int b;
+            int64_t i_in_seq;
+            bool bad_len = false;
+            if (a.cu_q_lens != nullptr) {
+                b = seq_of_token(a.cu_q_lens, B, t);
+                const int64_t first = ld_nc_s32(a.cu_q_lens + b);
+                const int64_t next = ld_nc_s32(a.cu_q_lens + b + 1);
+                i_in_seq = t - first;
+                bad_len = !(first <= t && t < next);
+            } else {
+                b = (int)t;
+                i_in_seq = 0;
+            }
+            const int64_t ctx = ld_nc_s32(a.context_kv_lens + b);
+            const int64_t pos = ctx + i_in_seq;
+            int64_t lb;
+            if (pos >= 0 && pos <= 0x7FFFFFFF) {
+                lb = (int64_t)((uint32_t)pos / (uint32_t)bs);
+            } else {
+                lb = pos / bs;
+            }
+            int32_t err = 0;
+            int32_t blk = 0;
+            if (bad_len || ctx < 0) {
+                err = KVC8_DEV_BAD_LENGTH;
+            } else if (lb >= MB) {
+                err = KVC8_DEV_POS_BEYOND_TABLE;
+            } else {
+                blk = ld_nc_s32(a.block_table + (int64_t)b * MB + lb);
+                if (blk < 0 || blk >= NB) err = KVC8_DEV_BAD_BLOCK_ID;
+            }
+            if (err != 0) {
+                if (lane == 0 && p0 == 0) report(a.dev_error, err);
+                break;  // warp-uniform: skip the token
+            }
+            const int64_t slot = pos - lb * bs;
+
+            // ---- quantise and scatter ----
 #pragma unroll
-            for (int k = 0; k < kGroup; ++k) {
+            for (int k = 0; k < G; ++k) {
                 if (p0 + k >= passes) break;  // warp-uniform
                 const int row = (p0 + k) * RPP + sub;
-                const bool row_on = row < rows;
+                const bool on = row < rows && lane_on;
                 const int kv = row >= H;
                 const int h = row - kv * H;
-                const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
-                float x[8];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    x[2 * j] = bf16_lo(w[j]);
-                    x[2 * j + 1] = bf16_hi(w[j]);
-                }
-                int q[8];
-                float s_row = 0.0f;
-                unsigned near_mask = 0;
+
+                float s_row = 0.0f, r_row = 0.0f;
                 if (MODE == 0) {
-                    // |x| ordering equals the ordering of the magnitude bits.
-                    uint32_t m2 = __vmaxu2(__vmaxu2(w[0] & 0x7FFF7FFFu, w[1] & 0x7FFF7FFFu),
-                                           __vmaxu2(w[2] & 0x7FFF7FFFu, w[3] & 0x7FFF7FFFu));
+                    // |x| ordering equals the ordering of the magnitude bits
+                    uint32_t m2 = 0;
+#pragma unroll
+                    for (int i = 0; i < W; ++i) m2 = __vmaxu2(m2, w[k][i] & 0x7FFF7FFFu);
                     uint32_t mag = max(m2 & 0xFFFFu, m2 >> 16);
 #pragma unroll
                     for (int o = 1; o < LANES; o <<= 1)
                         mag = max(mag, __shfl_xor_sync(0xFFFFFFFFu, mag, o));
-                    const float amax = __uint_as_float(mag << 16);
-                    s_row = __fdiv_rn(amax, 127.0f);
-                    const bool fast = recip_ok(s_row);
-                    const float r = fast ? __frcp_rn(s_row) : 0.0f;
+                    s_row = __fdiv_rn(__uint_as_float(mag << 16), 127.0f);
+                    r_row = recip_ok(s_row) ? __frcp_rn(s_row) : 0.0f;
+                }
+                const float *rt = r_tab + (kv * H + h) * D + c * E;
+                const float *st = s_tab + (kv * H + h) * D + c * E;
+
+                uint32_t cw[W / 2];  // packed codes, four per word
+                float dmax = 0.0f;
+                const u64 rr0 = pk(r_row, r_row);
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        bool nr;
-                        q[j] = quant_fast(x[j], r, nr);
-                        near_mask |= (unsigned)(nr || !fast) << j;
+                for (int i = 0; i < W; i += 2) {
+                    uint32_t mbits[4];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const uint32_t wi = w[k][i + e];
+                        const u64 x2 = pk(__uint_as_float(wi << 16), __uint_as_float(wi & 0xFFFF0000u));
+                        u64 y2;
+                        if (MODE == 0) {
+                            y2 = mul2(x2, rr0);  // |y| <= 127.00003: no clamp needed
+                        } else {
+                            const float2 r2 = on ? *reinterpret_cast<const float2 *>(rt + 2 * (i + e))
+                                                 : make_float2(1.0f, 1.0f);
+                            float ylo, yhi;
+                            upk(mul2(x2, pk(r2.x, r2.y)), ylo, yhi);
+                            y2 = pk(fminf(fmaxf(ylo, -kSatClamp), kSatClamp),
+                                    fminf(fmaxf(yhi, -kSatClamp), kSatClamp));
+                        }
+                        const u64 m2 = add2(y2, magic2);
+                        const u64 d2 = fma2(add2(m2, nmagic2), neg1, y2);  // y - rne(y), exact
+                        float dlo, dhi, mlo, mhi;
+                        upk(d2, dlo, dhi);
+                        upk(m2, mlo, mhi);
+                        dmax = fmaxf(dmax, fmaxf(fabsf(dlo), fabsf(dhi)));
+                        mbits[2 * e] = __float_as_uint(mlo);  // low byte = code
+                        mbits[2 * e + 1] = __float_as_uint(mhi);
                     }
-                    if (near_mask) {
+                    cw[i / 2] = pack_lo_bytes(mbits[0], mbits[1], mbits[2], mbits[3]);
+                }
+                const bool slow = (MODE == 0) ? (dmax >= kNearTie || r_row == 0.0f)
+                                              : (dmax >= kNearTie || !all_fast);
+                if (slow && on) {
+                    // recompute this lane's values one by one, exact where needed
 #pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            if (near_mask & (1u << j)) q[j] = quant_exact(x[j], s_row);
-                    }
-                } else {
-                    const int base = (kv * H + h) * D + c * 8;
-                    float r[8];
-                    if (lane_on && row_on) {
-                        const float4 r0 = *reinterpret_cast<const float4 *>(r_tab + base);
-                        const float4 r1 = *reinterpret_cast<const float4 *>(r_tab + base + 4);
-                        r[0] = r0.x; r[1] = r0.y; r[2] = r0.z; r[3] = r0.w;
-                        r[4] = r1.x; r[5] = r1.y; r[6] = r1.z; r[7] = r1.w;
-                    } else {
+                    for (int i = 0; i < W; i += 2) {
+                        int q[4];
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) r[j] = 1.0f;
-                    }
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        bool nr;
-                        q[j] = quant_fast(x[j], r[j], nr);
-                        near_mask |= (unsigned)(nr || r[j] == 0.0f) << j;
-                    }
-                    if (near_mask && lane_on && row_on) {
-#pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            if (near_mask & (1u << j)) q[j] = quant_exact(x[j], s_tab[base + j]);
+                        for (int e = 0; e < 4; ++e) {
+                            const uint32_t wi = w[k][i + (e >> 1)];
+                            const float x = __uint_as_float((e & 1) ? (wi & 0xFFFF0000u) : (wi << 16));
+                            const int j = 2 * i + e;
+                            q[e] = quant_one(x, MODE == 0 ? s_row : st[j], MODE == 0 ? r_row : rt[j]);
+                        }
+                        cw[i / 2] = pack_lo_bytes((uint32_t)q[0], (uint32_t)q[1], (uint32_t)q[2],
+                                                  (uint32_t)q[3]);
                     }
                 }
-                if (row_on && lane_on) {
+                if (on) {
                     int8_t *cache = kv ? a.v_cache : a.k_cache;
                     const int64_t dst_row = ((int64_t)blk * H + h) * bs + slot;
-                    st_8(cache + dst_row * D + c * 8, pack4(q[0], q[1], q[2], q[3]),
-                         pack4(q[4], q[5], q[6], q[7]));
+                    int8_t *dst = cache + dst_row * D + c * E;
+                    if (E == 32) store_codes32<V32>(dst, cw);
+                    else store_codes16(dst, cw);
                     if (MODE == 0 && c == 0) (kv ? a.v_scale : a.k_scale)[dst_row] = s_row;
                 }
             }
@@ -226,12 +323,17 @@ store_kernel(const StoreArgs a) {
     }
 }
 
-template <int LANES, int MODE>
+struct OccCache {
+    int dev = -1;
+    size_t smem = 0;
+    int occ = 0;
+};
+
+template <int E, int LANES, int MODE, bool V32>
 cudaError_t launch_variant(const StoreArgs &a, cudaStream_t stream) {
-    auto kern = store_kernel<LANES, MODE>;
+    auto kern = store_kernel<E, LANES, MODE, V32>;
     const size_t smem = MODE == 1 ? sizeof(float) * 4 * a.g.kv_heads * a.g.head_dim : 0;
-    static int dev_cached[64];
-    static int occ_cached[64];
+    static OccCache cache;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -240,17 +342,16 @@ cudaError_t launch_variant(const StoreArgs &a, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
     }
     int occ = 0;
-    if (MODE == 0 && dev < 64 && dev_cached[dev]) {
-        occ = occ_cached[dev];
+    if (cache.dev == dev && cache.smem == smem) {
+        occ = cache.occ;
     } else {
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kWarpsPerCta * 32, smem);
         if (e != cudaSuccess) return e;
-        if (MODE == 0 && dev < 64) {
-            occ_cached[dev] = occ;
-            dev_cached[dev] = 1;
-        }
+        if (occ < 1) occ = 1;
+        cache.occ = occ;
+        cache.smem = smem;
+        cache.dev = dev;
     }
-    if (occ < 1) occ = 1;
     const int64_t need = (a.num_tokens + kWarpsPerCta - 1) / kWarpsPerCta;
     const int64_t cap = (int64_t)sm_count() * occ;
     const int grid = (int)(need < cap ? need : cap);
@@ -258,21 +359,36 @@ cudaError_t launch_variant(const StoreArgs &a, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
-template <int MODE>
+template <int MODE, bool V32>
 cudaError_t launch_mode(const StoreArgs &a, cudaStream_t stream) {
-    const int C = a.g.head_dim / 8;
-    if (C <= 2) return launch_variant<2, MODE>(a, stream);
-    if (C <= 4) return launch_variant<4, MODE>(a, stream);
-    if (C <= 8) return launch_variant<8, MODE>(a, stream);
-    if (C <= 16) return launch_variant<16, MODE>(a, stream);
-    return launch_variant<32, MODE>(a, stream);
+    const int D = a.g.head_dim;
+    if (D % 32 == 0) {
+        const int C = D / 32;  // 1..8
+        if (C <= 1) return launch_variant<32, 1, MODE, V32>(a, stream);
+        if (C <= 2) return launch_variant<32, 2, MODE, V32>(a, stream);
+        if (C <= 4) return launch_variant<32, 4, MODE, V32>(a, stream);
+        return launch_variant<32, 8, MODE, V32>(a, stream);
+    }
+    const int C = D / 16;  // odd multiples of 16: 1..15
+    if (C <= 1) return launch_variant<16, 1, MODE, V32>(a, stream);
+    if (C <= 2) return launch_variant<16, 2, MODE, V32>(a, stream);
+    if (C <= 4) return launch_variant<16, 4, MODE, V32>(a, stream);
+    if (C <= 8) return launch_variant<16, 8, MODE, V32>(a, stream);
+    return launch_variant<16, 16, MODE, V32>(a, stream);
 }
+
+bool aligned32(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 31) == 0; }
 
 }  // namespace
 
 cudaError_t launch_store(const StoreArgs &a, cudaStream_t stream) {
     if (a.num_tokens <= 0) return cudaSuccess;
-    return a.g.quant_mode == 0 ? launch_mode<0>(a, stream) : launch_mode<1>(a, stream);
+    const bool v32 = aligned32(a.k_states) && aligned32(a.v_states) && aligned32(a.k_cache) &&
+                     aligned32(a.v_cache) && a.x_tok_stride % 16 == 0 &&
+                     a.x_head_stride % 16 == 0;
+    if (a.g.quant_mode == 0)
+        return v32 ? launch_mode<0, true>(a, stream) : launch_mode<0, false>(a, stream);
+    return v32 ? launch_mode<1, true>(a, stream) : launch_mode<1, false>(a, stream);
 }
 
 }  // namespace kvc8

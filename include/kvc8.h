@@ -203,7 +203,9 @@ kvc8_status kvc8_build_metadata(const kvc8_geom *g, const int32_t *context_lengt
  *   context_lengths          int32 [B]
  *   context_seq_offset       int64 [B] or NULL (exclusive prefix sum)
  *   key_out, value_out       bf16, rows [0, out_rows)
- *   workspace                as in kvc8_build_metadata
+ *   workspace                as in kvc8_build_metadata; also holds the gather's
+ *                            work counter, so calls that overlap on the GPU need
+ *                            separate workspaces
  */
 kvc8_status kvc8_dequant_gather(const kvc8_geom *g, const int8_t *key_cache,
                                 const int8_t *value_cache, const float *key_scale,
@@ -219,7 +221,10 @@ kvc8_status kvc8_dequant_gather(const kvc8_geom *g, const int8_t *key_cache,
  * kvc8_dequant_gather_planned -- kvc8_dequant_gather with a plan that an earlier
  * kvc8_build_metadata wrote into `workspace` for the same context lengths,
  * offsets and geometry (e.g. reused across the layers of one model step).
- * One launch.  Arguments as in kvc8_dequant_gather.
+ * One launch (after an 8-byte memset of the plan's work counter: the gather
+ * hands out its work through an atomic counter kept in the workspace, so two
+ * gathers that overlap on the GPU must not share a workspace).  Arguments as
+ * in kvc8_dequant_gather.
  */
 kvc8_status kvc8_dequant_gather_planned(const kvc8_geom *g, const int8_t *key_cache,
                                         const int8_t *value_cache,
@@ -228,7 +233,7 @@ kvc8_status kvc8_dequant_gather_planned(const kvc8_geom *g, const int8_t *key_ca
                                         const int32_t *context_lengths, void *key_out,
                                         void *value_out, int64_t out_rows,
                                         int64_t out_tok_stride, int64_t out_head_stride,
-                                        const void *workspace, size_t workspace_bytes,
+                                        void *workspace, size_t workspace_bytes,
                                         int32_t *dev_error, cudaStream_t stream);
 
 /*
