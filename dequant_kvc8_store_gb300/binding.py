@@ -59,6 +59,30 @@ def declared_functions() -> list:
     return sorted(set(re.findall(r"\b(kvc8_\w+)\s*\(", text)))
 
 
+def configure(lib: ctypes.CDLL) -> ctypes.CDLL:
+    """Declare the C signatures of kvc8.h on a loaded copy of the library."""
+    P, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+    G = ctypes.POINTER(Geom)
+    lib.kvc8_status_str.argtypes = [ctypes.c_int]
+    lib.kvc8_status_str.restype = ctypes.c_char_p
+    lib.kvc8_version.argtypes = []
+    lib.kvc8_version.restype = i32
+    lib.kvc8_store.argtypes = [G, i64, P, P, i64, i64, P, P, P, P, P, P, P, P, P]
+    lib.kvc8_store.restype = ctypes.c_int
+    lib.kvc8_gather_workspace_bytes.argtypes = [G]
+    lib.kvc8_gather_workspace_bytes.restype = sz
+    lib.kvc8_build_metadata.argtypes = [G, P, P, P, P, sz, P, P]
+    lib.kvc8_build_metadata.restype = ctypes.c_int
+    lib.kvc8_dequant_gather.argtypes = [G, P, P, P, P, P, P, P, P, P, i64, i64, i64, P, sz, P, P]
+    lib.kvc8_dequant_gather.restype = ctypes.c_int
+    lib.kvc8_dequant_gather_planned.argtypes = [G, P, P, P, P, P, P, P, P, i64, i64, i64, P, sz,
+                                                P, P]
+    lib.kvc8_dequant_gather_planned.restype = ctypes.c_int
+    lib.kvc8_get_error.argtypes = [P, ctypes.POINTER(ctypes.c_int32), i32, P]
+    lib.kvc8_get_error.restype = ctypes.c_int
+    return lib
+
+
 def load(build_if_needed: bool = True) -> ctypes.CDLL:
     """Load libkvc8.so (building it with nvcc first if it is missing or stale)."""
     global _lib
@@ -68,29 +92,8 @@ def load(build_if_needed: bool = True) -> ctypes.CDLL:
         path = _build.build() if build_if_needed else _build.LIB_PATH
         if not os.path.exists(path):
             raise ImportError(f"libkvc8 is not built ({path}); run dequant_kvc8_store_gb300/buildlib.py")
-        lib = ctypes.CDLL(path)
-        P, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
-        G = ctypes.POINTER(Geom)
-        lib.kvc8_status_str.argtypes = [ctypes.c_int]
-        lib.kvc8_status_str.restype = ctypes.c_char_p
-        lib.kvc8_version.argtypes = []
-        lib.kvc8_version.restype = i32
-        lib.kvc8_store.argtypes = [G, i64, P, P, i64, i64, P, P, P, P, P, P, P, P, P]
-        lib.kvc8_store.restype = ctypes.c_int
-        lib.kvc8_gather_workspace_bytes.argtypes = [G]
-        lib.kvc8_gather_workspace_bytes.restype = sz
-        lib.kvc8_build_metadata.argtypes = [G, P, P, P, P, sz, P, P]
-        lib.kvc8_build_metadata.restype = ctypes.c_int
-        lib.kvc8_dequant_gather.argtypes = [G, P, P, P, P, P, P, P, P, P, i64, i64, i64, P, sz,
-                                            P, P]
-        lib.kvc8_dequant_gather.restype = ctypes.c_int
-        lib.kvc8_dequant_gather_planned.argtypes = [G, P, P, P, P, P, P, P, P, i64, i64, i64,
-                                                    P, sz, P, P]
-        lib.kvc8_dequant_gather_planned.restype = ctypes.c_int
-        lib.kvc8_get_error.argtypes = [P, ctypes.POINTER(ctypes.c_int32), i32, P]
-        lib.kvc8_get_error.restype = ctypes.c_int
-        _lib = lib
-        return lib
+        _lib = configure(ctypes.CDLL(path))
+        return _lib
 
 
 def status_name(status: int) -> str:

@@ -12,8 +12,9 @@
 // and handed to a persistent grid through an atomic counter, so every CTA keeps
 // streaming equal-sized items however ragged the sequence lengths are.  Inside
 // an item each thread moves chunks of 32 codes (256-bit loads; 16 when D is not
-// a multiple of 32) -> 64 bytes of bf16, two chunks per slab, so four loads
-// (128 bytes) are in flight per thread.  Source reads and destination writes
+// a multiple of 32) -> 64 bytes of bf16, one chunk per slab per round, so two
+// loads are in flight per thread and the low register count keeps many CTAs
+// resident.  Source reads and destination writes
 // are both fully coalesced without a shared-memory transpose, because the
 // transpose [heads, tokens, dim] -> [tokens, heads, dim] only permutes whole
 // D-element rows.
@@ -199,7 +200,7 @@ template <int MODE, int CH, bool WIDE>
 __global__ void __launch_bounds__(kGatherThreads)
 gather_kernel(const GatherArgs a) {
     constexpr int W = CH / 4;  // words per chunk
-    constexpr int PER = 2;     // chunks per slab per thread per round
+    constexpr int PER = 1;     // chunks per slab per thread per round
     const int H = a.g.kv_heads, D = a.g.head_dim, bs = a.g.block_size;
     const int B = a.g.num_seqs, MB = a.g.max_blocks_per_seq, NB = a.g.num_blocks;
     const int CPR = D / CH;  // chunks per row

@@ -8,14 +8,19 @@
 // up to a power of two) cover a row and a warp pass covers 32/LANES rows.  The
 // row data of a token is requested before its slot is computed, so the
 // metadata lookups overlap the loads.  The grid is persistent (a multiple of
-// the SM count) and warps stride over tokens.
+// the SM count) and warps stride over tokens.  The kernel is bound by issue
+// slots rather than by HBM, so the per-value work is kept to a few packed
+// fp32x2 operations (see below).
 //
 // Rounding is bit-exact with the definition q = clamp(rne(x / s), -127, 127)
 // (one IEEE fp32 division).  Per element the kernel evaluates y = x * r with
 // r = fl(1/s) (correctly rounded), in packed fp32x2 arithmetic.  The relative
 // error of y against the exact quotient t = x/s is at most 2^-23 + 2^-48, so
 // |y - t| < 1.55e-5 whenever |t| <= 130; fl(t) is within half an ulp of t
-// (<= 7.7e-6 below 256).  If y lies more than 2^-15 (3.05e-5) from every
+// (<= 7.7e-6 below 256).  In dynamic mode y is never rounded on its own: one
+// fused multiply-add gives m = fl(x*r + 1.5*2^23) = 1.5*2^23 + rne(x*r) from
+// the exact product, and a second one the residual d = fl(x*r - rne(x*r)), so
+// there |y - t| <= 7.6e-6 and the margin below is wider still.  If y lies more than 2^-15 (3.05e-5) from every
 // half-integer, then t and fl(t) lie strictly inside the same interval between
 // half-integers as y, and rne(y) = rne(fl(t)).  y is rounded by adding
 // 1.5 * 2^23 (RNE to an integer, whose low byte is the code).  A lane whose
@@ -35,33 +40,6 @@ constexpr int kWarpsPerCta = 8;
 constexpr float kMagic = 12582912.0f;            // 1.5 * 2^23
 constexpr float kNearTie = 0.499969482421875f;   // 0.5 - 2^-15
 constexpr float kSatClamp = 127.0f;   // |y| >= 127 gives +-127 on both paths
-
-typedef unsigned long long u64;
-
-__device__ __forceinline__ u64 pk(float lo, float hi) {
-    u64 r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-    return r;
-}
-__device__ __forceinline__ void upk(u64 v, float &lo, float &hi) {
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-__device__ __forceinline__ u64 mul2(u64 a, u64 b) {
-    u64 r;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-__device__ __forceinline__ u64 add2(u64 a, u64 b) {
-    u64 r;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-// a * b + c, one rounding per lane
-__device__ __forceinline__ u64 fma2(u64 a, u64 b, u64 c) {
-    u64 r;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-    return r;
-}
 
 // Reciprocal fast path needs s and 1/s normal and finite.
 __device__ __forceinline__ bool recip_ok(float s) {
@@ -153,13 +131,24 @@ store_kernel(const StoreArgs a) {
     const int c = lane % LANES;
     const bool lane_on = c < C;
 
-    // Static mode: scale and reciprocal tables [2][H][D] in shared memory; a
-    // zero reciprocal marks a scale that must take the exact path.
+    // Shared tables.  Dynamic mode: for a bf16 row maximum amax = (1 + m/128)
+    // * 2^E, s = fl(amax / 127) = fl((1 + m/128) / 127) * 2^E and
+    // 1/s rounds to fl(1 / that) * 2^-E exactly, as long as both stay normal;
+    // the tables hold the two fl() values for the 128 mantissas.  Static mode:
+    // scale and reciprocal tables [2][H][D]; a zero reciprocal marks a scale
+    // that must take the exact path.
     extern __shared__ float smem[];
     float *s_tab = smem;
-    float *r_tab = smem + 2 * H * D;
+    float *r_tab = smem + (MODE == 0 ? 128 : 2 * H * D);
     bool all_fast = true;
-    if (MODE == 1) {
+    if (MODE == 0) {
+        for (int m = threadIdx.x; m < 128; m += blockDim.x) {
+            const float sm = __fdiv_rn(__uint_as_float(0x3F800000u | ((uint32_t)m << 16)), 127.0f);
+            s_tab[m] = sm;
+            r_tab[m] = __frcp_rn(sm);
+        }
+        __syncthreads();
+    } else {
         int ok = 1;
         for (int i = threadIdx.x; i < 2 * H * D; i += blockDim.x) {
             float s = i < H * D ? ld_nc_f32(a.k_scale + i) : ld_nc_f32(a.v_scale + (i - H * D));
@@ -174,9 +163,9 @@ store_kernel(const StoreArgs a) {
     const int rows = 2 * H;
     const int passes = (rows + RPP - 1) / RPP;
     const int64_t nwarps = (int64_t)gridDim.x * kWarpsPerCta;
-    const u64 magic2 = pk(kMagic, kMagic);
-    const u64 nmagic2 = pk(-kMagic, -kMagic);
-    const u64 neg1 = pk(-1.0f, -1.0f);
+    const float2 magic2 = make_float2(kMagic, kMagic);
+    const float2 nmagic2 = make_float2(-kMagic, -kMagic);
+    const float2 neg1 = make_float2(-1.0f, -1.0f);
 
     for (int64_t t = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5); t < a.num_tokens;
          t += nwarps) {
@@ -246,52 +235,62 @@ store_kernel(const StoreArgs a) {
 
                 float s_row = 0.0f, r_row = 0.0f;
                 if (MODE == 0) {
-                    // |x| ordering equals the ordering of the magnitude bits
-                    uint32_t m2 = 0;
+                    // |x| maximum: max(|a|, |b|) per bf16 half (the sign of the
+                    // result is garbage and masked off before comparing words)
+                    uint32_t m4[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-                    for (int i = 0; i < W; ++i) m2 = __vmaxu2(m2, w[k][i] & 0x7FFF7FFFu);
+                    for (int i = 0; i < W; ++i)
+                        asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(m4[i & 3]) : "r"(m4[i & 3]), "r"(w[k][i]));
+                    const uint32_t m2 = __vmaxu2(__vmaxu2(m4[0] & 0x7FFF7FFFu, m4[1] & 0x7FFF7FFFu),
+                                                 __vmaxu2(m4[2] & 0x7FFF7FFFu, m4[3] & 0x7FFF7FFFu));
                     uint32_t mag = max(m2 & 0xFFFFu, m2 >> 16);
 #pragma unroll
                     for (int o = 1; o < LANES; o <<= 1)
                         mag = max(mag, __shfl_xor_sync(0xFFFFFFFFu, mag, o));
-                    s_row = __fdiv_rn(__uint_as_float(mag << 16), 127.0f);
-                    r_row = recip_ok(s_row) ? __frcp_rn(s_row) : 0.0f;
+                    const uint32_t ef = mag >> 7;  // bf16 exponent field of amax
+                    if (ef >= 14 && ef <= 253) {   // s and 1/s normal and within recip_ok
+                        const int sh = ((int)ef - 127) << 23;
+                        s_row = __int_as_float(__float_as_int(s_tab[mag & 127]) + sh);
+                        r_row = __int_as_float(__float_as_int(r_tab[mag & 127]) - sh);
+                    } else {
+                        s_row = __fdiv_rn(__uint_as_float(mag << 16), 127.0f);
+                        r_row = 0.0f;  // exact path for the whole row
+                    }
                 }
                 const float *rt = r_tab + (kv * H + h) * D + c * E;
                 const float *st = s_tab + (kv * H + h) * D + c * E;
 
                 uint32_t cw[W / 2];  // packed codes, four per word
-                float dmax = 0.0f;
-                const u64 rr0 = pk(r_row, r_row);
+                float dmx[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // independent |d| maxima
+                const float2 rr0 = make_float2(r_row, r_row);
 #pragma unroll
                 for (int i = 0; i < W; i += 2) {
                     uint32_t mbits[4];
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
                         const uint32_t wi = w[k][i + e];
-                        const u64 x2 = pk(__uint_as_float(wi << 16), __uint_as_float(wi & 0xFFFF0000u));
-                        u64 y2;
+                        const float2 x2 = make_float2(__uint_as_float(wi << 16), __uint_as_float(wi & 0xFFFF0000u));
+                        float2 m2, d2;
                         if (MODE == 0) {
-                            y2 = mul2(x2, rr0);  // |y| <= 127.00003: no clamp needed
+                            // m = M + rne(x r) from the exact product; d = fl(x r - k)
+                            m2 = __ffma2_rn(x2, rr0, magic2);
+                            d2 = __ffma2_rn(x2, rr0, __ffma2_rn(m2, neg1, magic2));
                         } else {
                             const float2 r2 = on ? *reinterpret_cast<const float2 *>(rt + 2 * (i + e))
                                                  : make_float2(1.0f, 1.0f);
-                            float ylo, yhi;
-                            upk(mul2(x2, pk(r2.x, r2.y)), ylo, yhi);
-                            y2 = pk(fminf(fmaxf(ylo, -kSatClamp), kSatClamp),
-                                    fminf(fmaxf(yhi, -kSatClamp), kSatClamp));
+                            float2 y2 = __fmul2_rn(x2, r2);
+                            y2.x = fminf(fmaxf(y2.x, -kSatClamp), kSatClamp);
+                            y2.y = fminf(fmaxf(y2.y, -kSatClamp), kSatClamp);
+                            m2 = __fadd2_rn(y2, magic2);
+                            d2 = __ffma2_rn(__fadd2_rn(m2, nmagic2), neg1, y2);  // y - rne(y), exact
                         }
-                        const u64 m2 = add2(y2, magic2);
-                        const u64 d2 = fma2(add2(m2, nmagic2), neg1, y2);  // y - rne(y), exact
-                        float dlo, dhi, mlo, mhi;
-                        upk(d2, dlo, dhi);
-                        upk(m2, mlo, mhi);
-                        dmax = fmaxf(dmax, fmaxf(fabsf(dlo), fabsf(dhi)));
-                        mbits[2 * e] = __float_as_uint(mlo);  // low byte = code
-                        mbits[2 * e + 1] = __float_as_uint(mhi);
+                        dmx[((i >> 1) & 1) * 2 + e] = fmaxf(dmx[((i >> 1) & 1) * 2 + e], fmaxf(fabsf(d2.x), fabsf(d2.y)));
+                        mbits[2 * e] = __float_as_uint(m2.x);  // low byte = code
+                        mbits[2 * e + 1] = __float_as_uint(m2.y);
                     }
                     cw[i / 2] = pack_lo_bytes(mbits[0], mbits[1], mbits[2], mbits[3]);
                 }
+                const float dmax = fmaxf(fmaxf(dmx[0], dmx[1]), fmaxf(dmx[2], dmx[3]));
                 const bool slow = (MODE == 0) ? (dmax >= kNearTie || r_row == 0.0f)
                                               : (dmax >= kNearTie || !all_fast);
                 if (slow && on) {
@@ -332,7 +331,7 @@ struct OccCache {
 template <int E, int LANES, int MODE, bool V32>
 cudaError_t launch_variant(const StoreArgs &a, cudaStream_t stream) {
     auto kern = store_kernel<E, LANES, MODE, V32>;
-    const size_t smem = MODE == 1 ? sizeof(float) * 4 * a.g.kv_heads * a.g.head_dim : 0;
+    const size_t smem = MODE == 1 ? sizeof(float) * 4 * a.g.kv_heads * a.g.head_dim : sizeof(float) * 256;
     static OccCache cache;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
