@@ -8,6 +8,7 @@ from .binding import (DEV_BAD_BLOCK_ID, DEV_BAD_LENGTH, DEV_OK, DEV_OUT_ROW_RANG
                       DEV_POS_BEYOND_TABLE, ERR_CUDA, ERR_DEVICE_BOUNDS, ERR_INVALID_ARG,
                       ERR_UNSUPPORTED, ERR_WORKSPACE, OK, Geom, Kvc8Error,
                       declared_functions, kvc8_build_metadata, kvc8_dequant_gather,
-                      kvc8_dequant_gather_planned, kvc8_gather_workspace_bytes,
+                      kvc8_dequant_gather_noalloc, kvc8_dequant_gather_planned,
+                      kvc8_gather_workspace_bytes, NOALLOC_MAX_SEQS,
                       kvc8_get_error, kvc8_status_str, kvc8_store, kvc8_version, load)
 from .buildlib import build  # noqa: F401

@@ -80,6 +80,8 @@ def configure(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.kvc8_dequant_gather_planned.restype = ctypes.c_int
     lib.kvc8_get_error.argtypes = [P, ctypes.POINTER(ctypes.c_int32), i32, P]
     lib.kvc8_get_error.restype = ctypes.c_int
+    lib.kvc8_dequant_gather_noalloc.argtypes = [G, P, P, P, P, P, P, P, P, P, i64, i64, i64, P, P]
+    lib.kvc8_dequant_gather_noalloc.restype = ctypes.c_int
     return lib
 
 
@@ -181,6 +183,27 @@ def kvc8_dequant_gather_planned(g: Geom, key_cache, value_cache, key_scale, valu
                                             int(workspace_bytes), _p(dev_error),
                                             _stream(stream))
     _ok(st, "kvc8_dequant_gather_planned")
+
+
+NOALLOC_MAX_SEQS = 4096  # KVC8_NOALLOC_MAX_SEQS
+
+
+def kvc8_dequant_gather_noalloc(g: Geom, key_cache, value_cache, key_scale, value_scale,
+                                block_table, context_lengths, context_seq_offset, key_out,
+                                value_out, out_rows, out_tok_stride, out_head_stride,
+                                dev_error=None, stream=None) -> None:
+    """kvc8_dequant_gather without a workspace, for callers that cannot allocate
+    device memory: the plan lives in a fixed array inside the library (one per
+    device, shared by all calls, at most NOALLOC_MAX_SEQS sequences).  Make the
+    first call on a device before any stream capture; calls that overlap on the
+    GPU race on the shared array."""
+    st = load().kvc8_dequant_gather_noalloc(ctypes.byref(g), _p(key_cache), _p(value_cache),
+                                            _p(key_scale), _p(value_scale), _p(block_table),
+                                            _p(context_lengths), _p(context_seq_offset),
+                                            _p(key_out), _p(value_out), int(out_rows),
+                                            int(out_tok_stride), int(out_head_stride),
+                                            _p(dev_error), _stream(stream))
+    _ok(st, "kvc8_dequant_gather_noalloc")
 
 
 def kvc8_get_error(dev_error, reset: bool = False, stream=None) -> int:

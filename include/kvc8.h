@@ -236,6 +236,48 @@ kvc8_status kvc8_dequant_gather_planned(const kvc8_geom *g, const int8_t *key_ca
                                         void *workspace, size_t workspace_bytes,
                                         int32_t *dev_error, cudaStream_t stream);
 
+/* Largest num_seqs that kvc8_dequant_gather_noalloc accepts. */
+#define KVC8_NOALLOC_MAX_SEQS 4096
+
+/*
+ * kvc8_dequant_gather_noalloc -- kvc8_dequant_gather for callers that cannot
+ * allocate device memory.  The pages have no counterpart to this entry point;
+ * it exists for library users.
+ *
+ * Who needs it: code that runs inside a host runtime owning all device memory
+ * and offering its plugins no allocator, or a serving loop that must not
+ * allocate once it is running (an allocation can synchronise the device and
+ * upsets a memory plan fixed in advance).  Such a caller cannot provide the
+ * `workspace` that kvc8_dequant_gather needs.
+ *
+ * What it does instead: the gather's plan (offsets, tile prefix, work counter,
+ * about 50 KB) lives in one fixed device array inside the library, which every
+ * GPU that loads the library holds until the process exits.  The call
+ * allocates nothing (no cudaMalloc or cudaFree, no allocating library call);
+ * the caller still passes every input and output.  num_seqs above
+ * KVC8_NOALLOC_MAX_SEQS is rejected with KVC8_ERR_UNSUPPORTED before anything
+ * is enqueued.
+ *
+ * The first call on a device looks up that device's copy of the array
+ * (cudaGetSymbolAddress, with the device current) and remembers it; make that
+ * first call before any stream capture.  All calls on a device share the
+ * array: each call rewrites everything it reads from it, but calls whose work
+ * overlaps on the GPU (other streams, other host threads) race on it and must
+ * be serialised by the caller.
+ *
+ * Arguments, layouts and results are those of kvc8_dequant_gather, without
+ * the workspace pair.
+ */
+kvc8_status kvc8_dequant_gather_noalloc(const kvc8_geom *g, const int8_t *key_cache,
+                                        const int8_t *value_cache,
+                                        const float *key_scale, const float *value_scale,
+                                        const int32_t *block_table,
+                                        const int32_t *context_lengths,
+                                        const int64_t *context_seq_offset, void *key_out,
+                                        void *value_out, int64_t out_rows,
+                                        int64_t out_tok_stride, int64_t out_head_stride,
+                                        int32_t *dev_error, cudaStream_t stream);
+
 /*
  * kvc8_get_error -- synchronise `stream`, copy the device error word to
  * *host_code (host pointer) and return KVC8_ERR_DEVICE_BOUNDS if it is
