@@ -254,7 +254,8 @@ def run_e2e(args, w, d, dev, nbytes):
     out_v = torch.empty(d.v_out.shape, dtype=torch.bfloat16).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = out_k.numel() * 2 * 2
-    steps = max(3, min(args.steps, 50))
+    # bounded: at most ~16 GB of host<->device traffic, at least 3 steps
+    steps = max(3, min(args.steps, 50, int(16e9 // max(1, h2d + d2h))))
 
     def step():
         for name, t in host.items():
