@@ -205,10 +205,16 @@ gather_kernel(const GatherArgs a) {
     const int B = a.g.num_seqs, MB = a.g.max_blocks_per_seq, NB = a.g.num_blocks;
     const int CPR = D / CH;  // chunks per row
 
-    extern __shared__ float s_tab[];  // mode 1: static scales [2][H][D]
+    // Mode 1: static scales [2][H][D] as chunks of CH values padded by 4
+    // floats, so the chunk columns of a warp fall in different banks.
+    constexpr int SPAD = CH + 4;
+    extern __shared__ float s_tab[];
     if (MODE == 1) {
-        for (int i = threadIdx.x; i < 2 * H * D; i += blockDim.x)
-            s_tab[i] = i < H * D ? ld_nc_f32(a.k_scale + i) : ld_nc_f32(a.v_scale + (i - H * D));
+        for (int i = threadIdx.x; i < 2 * H * D; i += blockDim.x) {
+            const int row = i / D, d = i - row * D;
+            s_tab[(row * CPR + d / CH) * SPAD + d % CH] =
+                i < H * D ? ld_nc_f32(a.k_scale + i) : ld_nc_f32(a.v_scale + (i - H * D));
+        }
         __syncthreads();
     }
     __shared__ long long s_item;
@@ -255,7 +261,7 @@ gather_kernel(const GatherArgs a) {
                 const int h = u - kv * H;
                 src[sl] = (kv ? a.v_cache : a.k_cache) + ((int64_t)blk * H + h) * bs * D;
                 rsc[sl] = (kv ? a.v_scale : a.k_scale) + ((int64_t)blk * H + h) * bs;
-                csc[sl] = s_tab + (kv * H + h) * D;
+                csc[sl] = s_tab + (kv * H + h) * CPR * SPAD;
                 dst[sl] = (kv ? a.v_out : a.k_out) + row0 * a.out_tok_stride +
                           (int64_t)h * a.out_head_stride;
             }
@@ -286,7 +292,7 @@ gather_kernel(const GatherArgs a) {
                         const int row = c / CPR;
                         const int col = c - row * CPR;
                         uint32_t o[CH / 2];
-                        dequant_chunk<CH, MODE>(w[sl][k], s[sl][k], csc[sl] + col * CH, o);
+                        dequant_chunk<CH, MODE>(w[sl][k], s[sl][k], csc[sl] + col * SPAD, o);
                         store_chunk<CH, WIDE>(dst[sl] + (int64_t)row * a.out_tok_stride + col * CH, o);
                     }
                 }
@@ -302,7 +308,7 @@ gather_kernel(const GatherArgs a) {
 template <int MODE, int CH, bool WIDE>
 cudaError_t launch_gather_variant(const GatherArgs &a, bool use_pdl, cudaStream_t stream) {
     auto kern = gather_kernel<MODE, CH, WIDE>;
-    const size_t smem = MODE == 1 ? sizeof(float) * 2 * a.g.kv_heads * a.g.head_dim : 0;
+    const size_t smem = MODE == 1 ? sizeof(float) * 2 * a.g.kv_heads * (a.g.head_dim / CH) * (CH + 4) : 0;
     static int cached_dev = -1;
     static size_t cached_smem = 0;
     static int cached_occ = 0;

@@ -135,11 +135,14 @@ store_kernel(const StoreArgs a) {
     // * 2^E, s = fl(amax / 127) = fl((1 + m/128) / 127) * 2^E and
     // 1/s rounds to fl(1 / that) * 2^-E exactly, as long as both stay normal;
     // the tables hold the two fl() values for the 128 mantissas.  Static mode:
-    // scale and reciprocal tables [2][H][D]; a zero reciprocal marks a scale
-    // that must take the exact path.
+    // the reciprocal table [2][H][D], stored as chunks of E values (one per
+    // lane and row) padded by 2 floats so that the 32 lanes of a warp read
+    // different banks; a zero reciprocal marks a scale that must take the exact
+    // path (which reads the scale itself from global memory).
     extern __shared__ float smem[];
-    float *s_tab = smem;
-    float *r_tab = smem + (MODE == 0 ? 128 : 2 * H * D);
+    float *s_tab = smem;                           // dynamic mode only
+    float *r_tab = smem + (MODE == 0 ? 128 : 0);
+    constexpr int CHUNK = E + 2;                   // padded chunk stride (static mode)
     bool all_fast = true;
     if (MODE == 0) {
         for (int m = threadIdx.x; m < 128; m += blockDim.x) {
@@ -151,10 +154,10 @@ store_kernel(const StoreArgs a) {
     } else {
         int ok = 1;
         for (int i = threadIdx.x; i < 2 * H * D; i += blockDim.x) {
-            float s = i < H * D ? ld_nc_f32(a.k_scale + i) : ld_nc_f32(a.v_scale + (i - H * D));
-            s_tab[i] = s;
-            const bool f = recip_ok(s);
-            r_tab[i] = f ? __frcp_rn(s) : 0.0f;
+            const float sc = i < H * D ? ld_nc_f32(a.k_scale + i) : ld_nc_f32(a.v_scale + (i - H * D));
+            const bool f = recip_ok(sc);
+            const int row = i / D, d = i - row * D;
+            r_tab[(row * C + d / E) * CHUNK + d % E] = f ? __frcp_rn(sc) : 0.0f;
             ok &= f;
         }
         all_fast = __syncthreads_and(ok) != 0;
@@ -257,8 +260,8 @@ store_kernel(const StoreArgs a) {
                         r_row = 0.0f;  // exact path for the whole row
                     }
                 }
-                const float *rt = r_tab + (kv * H + h) * D + c * E;
-                const float *st = s_tab + (kv * H + h) * D + c * E;
+                const float *rt = r_tab + ((kv * H + h) * C + c) * CHUNK;                // static mode
+                const float *st = (kv ? a.v_scale : a.k_scale) + (int64_t)h * D + c * E;  // static mode
 
                 uint32_t cw[W / 2];  // packed codes, four per word
                 float dmx[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // independent |d| maxima
@@ -303,7 +306,7 @@ store_kernel(const StoreArgs a) {
                             const uint32_t wi = w[k][i + (e >> 1)];
                             const float x = __uint_as_float((e & 1) ? (wi & 0xFFFF0000u) : (wi << 16));
                             const int j = 2 * i + e;
-                            q[e] = quant_one(x, MODE == 0 ? s_row : st[j], MODE == 0 ? r_row : rt[j]);
+                            q[e] = quant_one(x, MODE == 0 ? s_row : ld_nc_f32(st + j), MODE == 0 ? r_row : rt[j]);
                         }
                         cw[i / 2] = pack_lo_bytes((uint32_t)q[0], (uint32_t)q[1], (uint32_t)q[2],
                                                   (uint32_t)q[3]);
@@ -331,7 +334,8 @@ struct OccCache {
 template <int E, int LANES, int MODE, bool V32>
 cudaError_t launch_variant(const StoreArgs &a, cudaStream_t stream) {
     auto kern = store_kernel<E, LANES, MODE, V32>;
-    const size_t smem = MODE == 1 ? sizeof(float) * 4 * a.g.kv_heads * a.g.head_dim : sizeof(float) * 256;
+    const int C = a.g.head_dim / E;
+    const size_t smem = MODE == 1 ? sizeof(float) * 2 * a.g.kv_heads * C * (E + 2) : sizeof(float) * 256;
     static OccCache cache;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
