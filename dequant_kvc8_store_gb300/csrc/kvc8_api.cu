@@ -92,6 +92,7 @@ kvc8_status kvc8_store(const kvc8_geom *g, int64_t num_tokens, const void *key_s
     kvc8_status st = check_geom(g);
     if (st != KVC8_OK) return st;
     if (num_tokens < 0) return KVC8_ERR_INVALID_ARG;
+    if (num_tokens > INT32_MAX) return KVC8_ERR_UNSUPPORTED;  // token indices are 32-bit
     if (cu_q_lens == nullptr && num_tokens != g->num_seqs) return KVC8_ERR_INVALID_ARG;
     if (num_tokens == 0 || g->num_seqs == 0) return num_tokens == 0 ? KVC8_OK : KVC8_ERR_INVALID_ARG;
     if (key_states == nullptr || value_states == nullptr || key_cache == nullptr ||

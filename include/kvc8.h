@@ -119,7 +119,7 @@ int32_t kvc8_version(void);
  * one launch, no host synchronisation.
  *
  *   g              geometry (host pointer)
- *   num_tokens     rows of key_states/value_states (N >= 0); 0 is a no-op
+ *   num_tokens     rows of key_states/value_states (0 <= N < 2^31); 0 is a no-op
  *   key_states,
  *   value_states   bf16 [N][H][D], strides (x_tok_stride, x_head_stride, 1)
  *                  in elements
