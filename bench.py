@@ -158,6 +158,32 @@ class ClockSampler:
                 "samples": len(rows)}
 
 
+# ---------------------------------------------------------------------------- ranks
+# One process per GPU.  The path has no exchange step: every rank stores and
+# gathers its own batch (its own seed), so the job scales weakly and the only
+# cross-rank traffic is the barrier and the max of the timings.
+
+def rank_seed(workload: str, rank: int) -> int:
+    """Seed of a rank's batch: the workload's own seed, shifted per rank."""
+    return 1000 + list(W.NAMED).index(workload) + 7919 * rank
+
+
+def reduce_max(values, device=None):
+    """Element-wise max of a list of floats over all ranks (no-op on one rank)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def job_throughput(bytes_per_rank_step: int, world: int, step_ms_max: float) -> float:
+    """Whole-job GB/s: the bytes all ranks moved in one step / the slowest rank's step."""
+    return world * bytes_per_rank_step / (step_ms_max * 1e-3) / 1e9
+
+
 # ---------------------------------------------------------------------------- GPU arm
 
 def run_gpu(args, rank, world):
@@ -168,7 +194,7 @@ def run_gpu(args, rank, world):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     kv.load()
-    w = W.NAMED[args.workload](seed=1000 + list(W.NAMED).index(args.workload) + 7919 * rank)
+    w = W.NAMED[args.workload](seed=rank_seed(args.workload, rank))
     nbytes = W.algorithmic_bytes(w)
     d = DeviceBatch(w, device=dev)
     stream = torch.cuda.current_stream()
@@ -224,11 +250,8 @@ def run_gpu(args, rank, world):
         raise RuntimeError("device error during the timed steps")
     local = {"step_ms": float(np.mean(step_ms)), "store_ms": float(np.mean(st_ms)),
              "gather_ms": float(np.mean(ga_ms)), "wall_s": wall}
-    if world > 1:
-        t = torch.tensor([local["step_ms"], local["store_ms"], local["gather_ms"]],
-                         dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        local["step_ms"], local["store_ms"], local["gather_ms"] = (float(x) for x in t.tolist())
+    local["step_ms"], local["store_ms"], local["gather_ms"] = reduce_max(
+        [local["step_ms"], local["store_ms"], local["gather_ms"]], device=dev)
     e2e = run_e2e(args, w, d, dev, nbytes) if rank == 0 else None
     return w, nbytes, local, clocks.summary(), e2e, has_store
 
@@ -359,7 +382,7 @@ def cpu_baseline(w: W.Workload, seconds: float = 12.0, per_pass_cap: float = 3.0
 def run_reference(args, rank, world):
     if rank != 0:
         return
-    w = W.NAMED[args.workload](seed=1000 + list(W.NAMED).index(args.workload))
+    w = W.NAMED[args.workload](seed=rank_seed(args.workload, 0))
     steps, warm = args.steps, args.warmup
     # each step a bounded sample, sized so the whole run stays within ~2 minutes
     per_step = min(2.0, 100.0 / max(1, steps + warm))
@@ -414,7 +437,7 @@ def main():
     if rank == 0:
         peak, peak_kind = measured_peak()
         total = nbytes["store"] + nbytes["gather"]
-        value = world * total / (t["step_ms"] * 1e-3) / 1e9
+        value = job_throughput(total, world, t["step_ms"])
         ops = {
             "store": {"ms": round(t["store_ms"], 5),
                       "GB_s": round(nbytes["store"] / (t["store_ms"] * 1e-3) / 1e9, 1) if has_store else None,
