@@ -122,6 +122,7 @@ kvc8_status kvc8_store(const kvc8_geom *g, int64_t num_tokens, const void *key_s
     a.cu_q_lens = cu_q_lens;
     a.context_kv_lens = context_kv_lens;
     a.dev_error = dev_error;
+    a.bs_magic = g->block_size >= 2 ? ~0ull / (unsigned long long)g->block_size + 1ull : 0ull;
     return cuda_status(launch_store(a, stream));
 }
 

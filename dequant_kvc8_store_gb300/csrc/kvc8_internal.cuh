@@ -114,6 +114,7 @@ struct StoreArgs {
     const int32_t *cu_q_lens;
     const int32_t *context_kv_lens;
     int32_t *dev_error;
+    unsigned long long bs_magic;  // ceil(2^64 / block_size) for block_size >= 2
 };
 
 struct GatherArgs {

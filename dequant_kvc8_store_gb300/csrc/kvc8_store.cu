@@ -13,24 +13,30 @@
 // fp32x2 operations (see below).
 //
 // Rounding is bit-exact with the definition q = clamp(rne(x / s), -127, 127)
-// (one IEEE fp32 division).  Per element the kernel evaluates y = x * r with
-// r = fl(1/s) (correctly rounded), in packed fp32x2 arithmetic.  The relative
-// error of y against the exact quotient t = x/s is at most 2^-23 + 2^-48, so
-// |y - t| < 1.55e-5 whenever |t| <= 130; fl(t) is within half an ulp of t
-// (<= 7.7e-6 below 256).  In dynamic mode y is never rounded on its own: one
-// fused multiply-add gives m = fl(x*r + 1.5*2^23) = 1.5*2^23 + rne(x*r) from
-// the exact product, and a second one the residual d = fl(x*r - rne(x*r)), so
-// there |y - t| <= 7.6e-6 and the margin below is wider still.  If y lies more than 2^-15 (3.05e-5) from every
-// half-integer, then t and fl(t) lie strictly inside the same interval between
-// half-integers as y, and rne(y) = rne(fl(t)).  y is rounded by adding
-// 1.5 * 2^23 (RNE to an integer, whose low byte is the code).  A lane whose
-// values come within 2^-15 of a half-integer (about 0.2% of 32-value lanes)
-// recomputes those values with __fdiv_rn + __float2int_rn.  In static mode y
-// is first clamped to [-127, 127]: |y| >= 127 means |t| >= 126.99998, whose
-// code is +-127 on both paths, and values below are untouched (in dynamic mode
-// |y| <= 127.00003 already).  Scales whose
-// reciprocal could leave the normal range (and zero scales) always take the
-// exact path.
+// (one IEEE fp32 division), without dividing in the common case.
+//
+// Dynamic mode (s = fl(amax/127), r = fl(1/s), both exact from 128-entry tables
+// indexed by the bf16 mantissa of amax): every value fl(x/s) can take lies
+// between x * r_lo and x * r_hi, with r_lo = fl(r (1 - 2^-21)) <= r (1 - 2^-23)
+// and r_hi >= r (1 + 2^-23), because r and fl(x/s) are each within a relative
+// 2^-24 of 1/s and x/s.  One fused multiply-add per end gives
+// 1.5*2^23 + rne(x r_lo) and 1.5*2^23 + rne(x r_hi) from the exact products
+// (|x r| <= 127.0001, so adding 1.5*2^23 rounds to an integer, ties to even,
+// and the low byte of the result is the code).  If the two agree, rne is
+// monotone, so rne(fl(x/s)) is that same integer.  If they differ (a value
+// within about 2^-21 relative of a half-integer; rare), the group of four
+// values is recomputed with __fdiv_rn + __float2int_rn.
+//
+// Static mode (s per channel; y = fl(x * fl(1/s)) clamped to [-127, 127]):
+// the relative error of y against t = x/s is at most 2^-23 + 2^-48, so
+// |y - t| < 1.55e-5 for |t| <= 130 and fl(t) is within half an ulp of t
+// (<= 7.7e-6 below 256).  If y lies more than 2^-15 from every half-integer,
+// t and fl(t) lie strictly inside the same interval between half-integers as
+// y and rne(y) = rne(fl(t)); otherwise the group takes the exact path.
+// |y| >= 127 means |t| >= 126.99998, whose code is +-127 either way.
+//
+// Scales whose reciprocal could leave the normal range (and zero scales)
+// always take the exact path.
 #include "kvc8_internal.cuh"
 
 namespace kvc8 {
@@ -68,12 +74,19 @@ __device__ __forceinline__ uint32_t pack_lo_bytes(uint32_t a, uint32_t b, uint32
     return __byte_perm(__byte_perm(a, b, 0x0040), __byte_perm(c, d, 0x0040), 0x5410);
 }
 
-// Largest b in [0, B] with cu[b] <= t (cu[0] = 0 <= t).
-__device__ __forceinline__ int seq_of_token(const int32_t *cu, int B, int64_t t) {
-    int lo = 0, hi = B;
+// Largest b in [0, B] with cu[b] <= t (cu[0] = 0 <= t < cu[B]), found by the
+// whole warp: each round samples 32 evenly spaced entries of the current range
+// at once and keeps the last sample <= t, so the range shrinks 32-fold per
+// round (two rounds for a thousand sequences).  All lanes get the same answer.
+__device__ __forceinline__ int seq_of_token(const int32_t *cu, int B, int64_t t, int lane) {
+    int lo = 0, hi = B;  // cu[lo] <= t < cu[hi]
     while (hi - lo > 1) {
-        int mid = (lo + hi) >> 1;
-        if ((int64_t)ld_nc_s32(cu + mid) <= t) lo = mid; else hi = mid;
+        const int step = (hi - lo + 31) >> 5;
+        const int idx = lo + step * (lane + 1);
+        const bool le = idx < hi && (int64_t)ld_nc_s32(cu + idx) <= t;
+        const unsigned m = __ballot_sync(0xFFFFFFFFu, le);
+        if (m != 0u) lo += step * (32 - __clz(m));
+        hi = min(hi, lo + step);
     }
     return lo;
 }
@@ -194,7 +207,7 @@ store_kernel(const StoreArgs a) {
             int64_t i_in_seq;
             bool bad_len = false;
             if (a.cu_q_lens != nullptr) {
-                b = seq_of_token(a.cu_q_lens, B, t);
+                b = seq_of_token(a.cu_q_lens, B, t, lane);
                 const int64_t first = ld_nc_s32(a.cu_q_lens + b);
                 const int64_t next = ld_nc_s32(a.cu_q_lens + b + 1);
                 i_in_seq = t - first;
@@ -205,9 +218,11 @@ store_kernel(const StoreArgs a) {
             }
             const int64_t ctx = ld_nc_s32(a.context_kv_lens + b);
             const int64_t pos = ctx + i_in_seq;
+            // pos < 2^32 always (ctx and the token index are below 2^31):
+            // floor(pos / bs) is the high word of pos * ceil(2^64 / bs)
             int64_t lb;
-            if (pos >= 0 && pos <= 0x7FFFFFFF) {
-                lb = (int64_t)((uint32_t)pos / (uint32_t)bs);
+            if (pos >= 0 && pos <= 0xFFFFFFFFll) {
+                lb = bs == 1 ? pos : (int64_t)__umul64hi(a.bs_magic, (unsigned long long)pos);
             } else {
                 lb = pos / bs;
             }
@@ -227,17 +242,13 @@ store_kernel(const StoreArgs a) {
             }
             const int64_t slot = pos - lb * bs;
 
-            // ---- quantise and scatter ----
+            // ---- row scales of every pass first (independent chains) ----
+            float s_rows[G], r_rows[G];
 #pragma unroll
             for (int k = 0; k < G; ++k) {
-                if (p0 + k >= passes) break;  // warp-uniform
-                const int row = (p0 + k) * RPP + sub;
-                const bool on = row < rows && lane_on;
-                const int kv = row >= H;
-                const int h = row - kv * H;
-
-                float s_row = 0.0f, r_row = 0.0f;
-                if (MODE == 0) {
+                s_rows[k] = 0.0f;
+                r_rows[k] = 0.0f;
+                if (MODE == 0 && p0 + k < passes) {
                     // |x| maximum: max(|a|, |b|) per bf16 half (the sign of the
                     // result is garbage and masked off before comparing words)
                     uint32_t m4[4] = {0u, 0u, 0u, 0u};
@@ -253,31 +264,51 @@ store_kernel(const StoreArgs a) {
                     const uint32_t ef = mag >> 7;  // bf16 exponent field of amax
                     if (ef >= 14 && ef <= 253) {   // s and 1/s normal and within recip_ok
                         const int sh = ((int)ef - 127) << 23;
-                        s_row = __int_as_float(__float_as_int(s_tab[mag & 127]) + sh);
-                        r_row = __int_as_float(__float_as_int(r_tab[mag & 127]) - sh);
+                        s_rows[k] = __int_as_float(__float_as_int(s_tab[mag & 127]) + sh);
+                        r_rows[k] = __int_as_float(__float_as_int(r_tab[mag & 127]) - sh);
                     } else {
-                        s_row = __fdiv_rn(__uint_as_float(mag << 16), 127.0f);
-                        r_row = 0.0f;  // exact path for the whole row
+                        s_rows[k] = __fdiv_rn(__uint_as_float(mag << 16), 127.0f);
+                        r_rows[k] = 0.0f;  // exact path for the whole row
                     }
                 }
+            }
+
+            // ---- quantise and scatter ----
+#pragma unroll
+            for (int k = 0; k < G; ++k) {
+                if (p0 + k >= passes) break;  // warp-uniform
+                const int row = (p0 + k) * RPP + sub;
+                const bool on = row < rows && lane_on;
+                const int kv = row >= H;
+                const int h = row - kv * H;
+                const float s_row = s_rows[k], r_row = r_rows[k];
                 const float *rt = r_tab + ((kv * H + h) * C + c) * CHUNK;                // static mode
                 const float *st = (kv ? a.v_scale : a.k_scale) + (int64_t)h * D + c * E;  // static mode
 
                 uint32_t cw[W / 2];  // packed codes, four per word
-                float dmx[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // independent |d| maxima
-                const float2 rr0 = make_float2(r_row, r_row);
+                const bool force_exact = (MODE == 0) ? (r_row == 0.0f) : !all_fast;
+                // Dynamic mode: r_lo <= r (1 - 2^-23) and r_hi >= r (1 + 2^-23)
+                // bracket every value fl(x / s) can take, so when x r_lo and
+                // x r_hi round to the same integer, so does fl(x / s).
+                const float2 rlo2 = make_float2(__fmul_rn(r_row, 0.99999952316284180f),
+                                                __fmul_rn(r_row, 0.99999952316284180f));
+                const float2 rhi2 = make_float2(__fmul_rn(r_row, 1.00000047683715820f),
+                                                __fmul_rn(r_row, 1.00000047683715820f));
 #pragma unroll
                 for (int i = 0; i < W; i += 2) {
                     uint32_t mbits[4];
+                    uint32_t differ = 0u;
+                    float dm = 0.0f;
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
                         const uint32_t wi = w[k][i + e];
                         const float2 x2 = make_float2(__uint_as_float(wi << 16), __uint_as_float(wi & 0xFFFF0000u));
-                        float2 m2, d2;
+                        float2 m2;
                         if (MODE == 0) {
-                            // m = M + rne(x r) from the exact product; d = fl(x r - k)
-                            m2 = __ffma2_rn(x2, rr0, magic2);
-                            d2 = __ffma2_rn(x2, rr0, __ffma2_rn(m2, neg1, magic2));
+                            m2 = __ffma2_rn(x2, rlo2, magic2);
+                            const float2 h2 = __ffma2_rn(x2, rhi2, magic2);
+                            differ |= (__float_as_uint(m2.x) ^ __float_as_uint(h2.x)) |
+                                      (__float_as_uint(m2.y) ^ __float_as_uint(h2.y));
                         } else {
                             const float2 r2 = on ? *reinterpret_cast<const float2 *>(rt + 2 * (i + e))
                                                  : make_float2(1.0f, 1.0f);
@@ -285,21 +316,16 @@ store_kernel(const StoreArgs a) {
                             y2.x = fminf(fmaxf(y2.x, -kSatClamp), kSatClamp);
                             y2.y = fminf(fmaxf(y2.y, -kSatClamp), kSatClamp);
                             m2 = __fadd2_rn(y2, magic2);
-                            d2 = __ffma2_rn(__fadd2_rn(m2, nmagic2), neg1, y2);  // y - rne(y), exact
+                            const float2 d2 = __ffma2_rn(__fadd2_rn(m2, nmagic2), neg1, y2);  // y - rne(y), exact
+                            dm = fmaxf(dm, fmaxf(fabsf(d2.x), fabsf(d2.y)));
                         }
-                        dmx[((i >> 1) & 1) * 2 + e] = fmaxf(dmx[((i >> 1) & 1) * 2 + e], fmaxf(fabsf(d2.x), fabsf(d2.y)));
                         mbits[2 * e] = __float_as_uint(m2.x);  // low byte = code
                         mbits[2 * e + 1] = __float_as_uint(m2.y);
                     }
-                    cw[i / 2] = pack_lo_bytes(mbits[0], mbits[1], mbits[2], mbits[3]);
-                }
-                const float dmax = fmaxf(fmaxf(dmx[0], dmx[1]), fmaxf(dmx[2], dmx[3]));
-                const bool slow = (MODE == 0) ? (dmax >= kNearTie || r_row == 0.0f)
-                                              : (dmax >= kNearTie || !all_fast);
-                if (slow && on) {
-                    // recompute this lane's values one by one, exact where needed
-#pragma unroll
-                    for (int i = 0; i < W; i += 2) {
+                    uint32_t word = pack_lo_bytes(mbits[0], mbits[1], mbits[2], mbits[3]);
+                    const bool near = (MODE == 0) ? (differ != 0u) : (dm >= kNearTie);
+                    if ((near || force_exact) && on) {
+                        // rare: recompute these four codes one by one, exact where needed
                         int q[4];
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
@@ -308,9 +334,9 @@ store_kernel(const StoreArgs a) {
                             const int j = 2 * i + e;
                             q[e] = quant_one(x, MODE == 0 ? s_row : ld_nc_f32(st + j), MODE == 0 ? r_row : rt[j]);
                         }
-                        cw[i / 2] = pack_lo_bytes((uint32_t)q[0], (uint32_t)q[1], (uint32_t)q[2],
-                                                  (uint32_t)q[3]);
+                        word = pack_lo_bytes((uint32_t)q[0], (uint32_t)q[1], (uint32_t)q[2], (uint32_t)q[3]);
                     }
+                    cw[i / 2] = word;
                 }
                 if (on) {
                     int8_t *cache = kv ? a.v_cache : a.k_cache;
