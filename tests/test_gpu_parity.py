@@ -105,6 +105,11 @@ SMALL = [
          block_size=64, num_blocks=300, quant_mode=1),
     dict(q_lens=[129, 255, 1], ctx_before=[0, 1, 1023], kv_heads=8, head_dim=128,
          block_size=128, num_blocks=40, quant_mode=0, outlier_channels=4),
+    # K and V rows of a token above 4 KB (the unstaged store path)
+    dict(q_lens=[77, 3, 140], ctx_before=[5, 0, 60], kv_heads=16, head_dim=128,
+         block_size=32, num_blocks=30, quant_mode=0),
+    dict(q_lens=[41, 1, 70], ctx_before=[0, 9, 31], kv_heads=12, head_dim=256,
+         block_size=16, num_blocks=40, quant_mode=1),
 ]
 
 
