@@ -8,7 +8,9 @@ the whole hot path, through the C ABI of libkvc8.
 Default workload: "prefill" -- batch 16, prompts U{512..4096} into an empty
 cache, 8 kv heads x head_dim 128, block 128, 1024-block pool, dynamic
 per-token scales, N(0,1) K/V with 4 outlier channels per head (x20).  Other
-workloads: --workload tiny|decode|mixed|longctx.
+workloads: --workload tiny|decode|mixed|longctx.  --path bf16 runs the same
+step on the bf16 cache without quantisation (kvc8_store_bf16 +
+kvc8_gather_bf16) instead of the int8 one.
 
 Timing: W untimed warm-up steps, then exactly K steps.  L2 is flushed (a
 256 MiB write, then a 256 MiB read) before each timed kernel; each op is bracketed by CUDA events on
@@ -48,6 +50,7 @@ FLUSH_BYTES = 256 << 20
 METRIC = "achieved HBM GB/s (% of ~8 TB/s) and K+V tokens/s for store and dequant"
 KERNEL_SOURCES = ["dequant_kvc8_store_gb300/csrc/kvc8_store.cu",
                   "dequant_kvc8_store_gb300/csrc/kvc8_gather.cu",
+                  "dequant_kvc8_store_gb300/csrc/kvc8_bf16.cu",
                   "dequant_kvc8_store_gb300/csrc/kvc8_internal.cuh"]
 WORKLOAD_TEXT = {
     "tiny": "tiny round trip: batch 2, q {5,19} after {3,0} cached, 2 kv heads x 64, block 16, "
@@ -189,14 +192,17 @@ def job_throughput(bytes_per_rank_step: int, world: int, step_ms_max: float) -> 
 def run_gpu(args, rank, world):
     import torch
     import dequant_kvc8_store_gb300 as kv
-    from dequant_kvc8_store_gb300.device import DeviceBatch
+    from dequant_kvc8_store_gb300.device import Bf16Batch, DeviceBatch
 
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     kv.load()
     w = W.NAMED[args.workload](seed=rank_seed(args.workload, rank))
-    nbytes = W.algorithmic_bytes(w)
-    d = DeviceBatch(w, device=dev)
+    nbytes = path_bytes(w, args.path)
+    if args.path == "bf16":
+        d = Bf16Batch(w, device=dev, seed=rank_seed(args.workload, rank))
+    else:
+        d = DeviceBatch(w, device=dev)
     stream = torch.cuda.current_stream()
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     clean = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
@@ -342,8 +348,20 @@ def sub_workload(w: W.Workload, token_budget: int) -> W.Workload:
     return s
 
 
-def oracle_pass(w: W.Workload):
+def oracle_pass(w: W.Workload, path: str = "c8"):
     import oracle
+    if path == "bf16":
+        # a zero pool of the workload's shape: its prior bits do not change
+        # what the copy costs
+        shape = w.k_cache.shape
+        kc = np.zeros(shape, np.uint16)
+        vc = np.zeros(shape, np.uint16)
+        t0 = time.perf_counter()
+        if w.has_store:
+            cu = w.cu_q_lens if w.cu_q_lens is not None else np.arange(w.num_tokens + 1, dtype=np.int32)
+            oracle.store_bf16(w.k_states, w.v_states, kc, vc, w.block_table, cu, w.context_kv_lens)
+        oracle.gather_bf16(kc, vc, w.block_table, w.context_lengths)
+        return time.perf_counter() - t0
     kc, vc = w.k_cache, w.v_cache
     ks, vs = w.k_scale, w.v_scale
     t0 = time.perf_counter()
@@ -354,7 +372,12 @@ def oracle_pass(w: W.Workload):
     return time.perf_counter() - t0
 
 
-def cpu_baseline(w: W.Workload, seconds: float = 12.0, per_pass_cap: float = 3.0):
+def path_bytes(w: W.Workload, path: str) -> dict:
+    return W.algorithmic_bytes_bf16(w) if path == "bf16" else W.algorithmic_bytes(w)
+
+
+def cpu_baseline(w: W.Workload, path: str = "c8", seconds: float = 12.0,
+                 per_pass_cap: float = 3.0):
     """The oracle as it stands on one host core, on a bounded sample of the
     workload (whole passes when one pass is cheap enough)."""
     full = int(w.q_lens().sum() + w.context_lengths.astype(np.int64).sum())
@@ -362,15 +385,15 @@ def cpu_baseline(w: W.Workload, seconds: float = 12.0, per_pass_cap: float = 3.0
     s = w
     # shrink the sample until one pass takes at most per_pass_cap seconds
     probe = sub_workload(w, min(full, 20000))
-    t = oracle_pass(probe)
+    t = oracle_pass(probe, path)
     rate = (int(probe.q_lens().sum()) + int(probe.context_lengths.astype(np.int64).sum())) / max(t, 1e-9)
     if full / rate > per_pass_cap:
         budget = int(rate * per_pass_cap)
         s = sub_workload(w, budget)
-    bytes_pass = sum(W.algorithmic_bytes(s).values())
+    bytes_pass = sum(path_bytes(s, path).values())
     times, t_end = [], time.perf_counter() + seconds
     while time.perf_counter() < t_end or not times:
-        times.append(oracle_pass(s))
+        times.append(oracle_pass(s, path))
     gbs = bytes_pass / statistics.median(times) / 1e9
     sample = (f"{len(times)} oracle passes of {'the full workload' if s is w else 'its first %d sequences' % s.num_seqs} "
               f"({int(s.q_lens().sum())} stored + {int(s.context_lengths.astype(np.int64).sum())} "
@@ -387,20 +410,22 @@ def run_reference(args, rank, world):
     # each step a bounded sample, sized so the whole run stays within ~2 minutes
     per_step = min(2.0, 100.0 / max(1, steps + warm))
     probe = sub_workload(w, 4000)
-    t = oracle_pass(probe)
+    t = oracle_pass(probe, args.path)
     rate = (int(probe.q_lens().sum()) + int(probe.context_lengths.astype(np.int64).sum())) / max(t, 1e-9)
     s = sub_workload(w, max(64, int(rate * per_step)))
-    bytes_step = sum(W.algorithmic_bytes(s).values())
+    bytes_step = sum(path_bytes(s, args.path).values())
     for _ in range(warm):
-        oracle_pass(s)
-    times = [oracle_pass(s) for _ in range(steps)]
+        oracle_pass(s, args.path)
+    times = [oracle_pass(s, args.path) for _ in range(steps)]
     ms = 1e3 * sum(times) / len(times)
     value = bytes_step / (ms * 1e-3) / 1e9
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
         "n_gpus": world, "steps": steps, "warmup": warm, "ms_per_step": round(ms, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if args.path == "bf16" else "f32",
         "data": "synthetic", "config": {"workload": WORKLOAD_TEXT[args.workload],
+                                        "path": "bf16 cache, no quantisation" if args.path == "bf16" else "int8 cache",
                                         "sample_positions_per_step": int(s.q_lens().sum() + s.context_lengths.astype(np.int64).sum())},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": f"each step: oracle store+gather of the first {s.num_seqs} "
@@ -420,6 +445,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["kvc8", "reference"], default="kvc8")
     ap.add_argument("--workload", choices=list(W.NAMED), default="prefill")
+    ap.add_argument("--path", choices=["c8", "bf16"], default="c8",
+                    help="c8: the int8 cache (default); bf16: the cache without quantisation")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -453,13 +480,18 @@ def main():
         dom_bytes = nbytes["gather"] if dom == "dequant_gather" else nbytes["store"]
         dom_ms = t["gather_ms"] if dom == "dequant_gather" else t["store_ms"]
         achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
-        traffic = ncu_traffic(args.workload).get("gather_kernel" if dom == "dequant_gather" else "store_kernel")
+        kname = "gather" if dom == "dequant_gather" else "store"
+        if args.path == "bf16":
+            kname += "_bf16"
+        traffic = ncu_traffic(args.workload).get(kname + "_kernel")
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t["step_ms"], 5),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if args.path == "bf16" else "f32",
             "data": "synthetic",
             "config": {"workload": WORKLOAD_TEXT[args.workload],
+                       "path": "bf16 cache, no quantisation" if args.path == "bf16" else "int8 cache",
                        "l2": "flushed before each timed op (256 MiB write, then 256 MiB read)",
                        "hbm_frac_of_step": round(total / (t["step_ms"] * 1e-3) / 1e9 / peak, 4),
                        "tokens_per_s": {"store": ops["store"]["tokens_per_s"],
@@ -475,7 +507,7 @@ def main():
             "wall_s": round(t["wall_s"], 3),
         }
         if world == 1 and not args.no_cpu_baseline:
-            line["cpu_baseline"] = cpu_baseline(w)
+            line["cpu_baseline"] = cpu_baseline(w, args.path)
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch

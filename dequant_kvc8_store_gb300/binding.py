@@ -82,6 +82,10 @@ def configure(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.kvc8_get_error.restype = ctypes.c_int
     lib.kvc8_dequant_gather_noalloc.argtypes = [G, P, P, P, P, P, P, P, P, P, i64, i64, i64, P, P]
     lib.kvc8_dequant_gather_noalloc.restype = ctypes.c_int
+    lib.kvc8_store_bf16.argtypes = [G, i64, P, P, i64, i64, P, P, P, P, P, P, P]
+    lib.kvc8_store_bf16.restype = ctypes.c_int
+    lib.kvc8_gather_bf16.argtypes = [G, P, P, P, P, P, P, P, i64, i64, i64, P, sz, P, P]
+    lib.kvc8_gather_bf16.restype = ctypes.c_int
     return lib
 
 
@@ -204,6 +208,28 @@ def kvc8_dequant_gather_noalloc(g: Geom, key_cache, value_cache, key_scale, valu
                                             int(out_tok_stride), int(out_head_stride),
                                             _p(dev_error), _stream(stream))
     _ok(st, "kvc8_dequant_gather_noalloc")
+
+
+def kvc8_store_bf16(g: Geom, num_tokens, key_states, value_states, x_tok_stride, x_head_stride,
+                    key_cache, value_cache, block_table, cu_q_lens, context_kv_lens,
+                    dev_error=None, stream=None) -> None:
+    st = load().kvc8_store_bf16(ctypes.byref(g), int(num_tokens), _p(key_states),
+                                _p(value_states), int(x_tok_stride), int(x_head_stride),
+                                _p(key_cache), _p(value_cache), _p(block_table), _p(cu_q_lens),
+                                _p(context_kv_lens), _p(dev_error), _stream(stream))
+    _ok(st, "kvc8_store_bf16")
+
+
+def kvc8_gather_bf16(g: Geom, key_cache, value_cache, block_table, context_lengths,
+                     context_seq_offset, key_out, value_out, out_rows, out_tok_stride,
+                     out_head_stride, workspace, workspace_bytes, dev_error=None,
+                     stream=None) -> None:
+    st = load().kvc8_gather_bf16(ctypes.byref(g), _p(key_cache), _p(value_cache),
+                                 _p(block_table), _p(context_lengths), _p(context_seq_offset),
+                                 _p(key_out), _p(value_out), int(out_rows), int(out_tok_stride),
+                                 int(out_head_stride), _p(workspace), int(workspace_bytes),
+                                 _p(dev_error), _stream(stream))
+    _ok(st, "kvc8_gather_bf16")
 
 
 def kvc8_get_error(dev_error, reset: bool = False, stream=None) -> int:

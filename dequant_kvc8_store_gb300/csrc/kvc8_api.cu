@@ -219,6 +219,90 @@ kvc8_status kvc8_dequant_gather_planned(const kvc8_geom *g, const int8_t *key_ca
     return cuda_status(launch_gather(a, /*use_pdl=*/false, stream));
 }
 
+// Geometry checks for the bf16 cache (quant_mode is not used there).
+static kvc8_status check_geom_bf16(const kvc8_geom *g) {
+    if (g == nullptr) return KVC8_ERR_INVALID_ARG;
+    kvc8_geom q = *g;
+    q.quant_mode = 0;
+    return check_geom(&q);
+}
+
+kvc8_status kvc8_store_bf16(const kvc8_geom *g, int64_t num_tokens, const void *key_states,
+                            const void *value_states, int64_t x_tok_stride, int64_t x_head_stride,
+                            void *key_cache, void *value_cache, const int32_t *block_table,
+                            const int32_t *cu_q_lens, const int32_t *context_kv_lens,
+                            int32_t *dev_error, cudaStream_t stream) {
+    kvc8_status st = check_geom_bf16(g);
+    if (st != KVC8_OK) return st;
+    if (num_tokens < 0) return KVC8_ERR_INVALID_ARG;
+    if (num_tokens > INT32_MAX) return KVC8_ERR_UNSUPPORTED;
+    if (cu_q_lens == nullptr && num_tokens != g->num_seqs) return KVC8_ERR_INVALID_ARG;
+    if (num_tokens == 0 || g->num_seqs == 0) return num_tokens == 0 ? KVC8_OK : KVC8_ERR_INVALID_ARG;
+    if (key_states == nullptr || value_states == nullptr || key_cache == nullptr ||
+        value_cache == nullptr || block_table == nullptr || context_kv_lens == nullptr)
+        return KVC8_ERR_INVALID_ARG;
+    if (x_tok_stride < 0 || x_head_stride < 0 || x_tok_stride % 8 != 0 || x_head_stride % 8 != 0)
+        return KVC8_ERR_INVALID_ARG;
+    if (!aligned(key_states, 16) || !aligned(value_states, 16) || !aligned(key_cache, 16) ||
+        !aligned(value_cache, 16))
+        return KVC8_ERR_INVALID_ARG;
+    StoreBf16Args a;
+    a.g = *g;
+    a.num_tokens = num_tokens;
+    a.k_states = static_cast<const uint16_t *>(key_states);
+    a.v_states = static_cast<const uint16_t *>(value_states);
+    a.x_tok_stride = x_tok_stride;
+    a.x_head_stride = x_head_stride;
+    a.k_cache = static_cast<uint16_t *>(key_cache);
+    a.v_cache = static_cast<uint16_t *>(value_cache);
+    a.block_table = block_table;
+    a.cu_q_lens = cu_q_lens;
+    a.context_kv_lens = context_kv_lens;
+    a.dev_error = dev_error;
+    return cuda_status(launch_store_bf16(a, stream));
+}
+
+kvc8_status kvc8_gather_bf16(const kvc8_geom *g, const void *key_cache, const void *value_cache,
+                             const int32_t *block_table, const int32_t *context_lengths,
+                             const int64_t *context_seq_offset, void *key_out, void *value_out,
+                             int64_t out_rows, int64_t out_tok_stride, int64_t out_head_stride,
+                             void *workspace, size_t workspace_bytes, int32_t *dev_error,
+                             cudaStream_t stream) {
+    kvc8_status st = check_geom_bf16(g);
+    if (st != KVC8_OK) return st;
+    if (g->num_seqs == 0) return KVC8_OK;
+    if (key_cache == nullptr || value_cache == nullptr || block_table == nullptr ||
+        context_lengths == nullptr || key_out == nullptr || value_out == nullptr)
+        return KVC8_ERR_INVALID_ARG;
+    if (out_rows < 0 || out_tok_stride < 0 || out_head_stride < 0 || out_tok_stride % 8 != 0 ||
+        out_head_stride % 8 != 0)
+        return KVC8_ERR_INVALID_ARG;
+    if (!aligned(key_out, 16) || !aligned(value_out, 16) || !aligned(key_cache, 16) ||
+        !aligned(value_cache, 16))
+        return KVC8_ERR_INVALID_ARG;
+    kvc8_geom q = *g;
+    q.quant_mode = 0;
+    st = check_workspace(&q, workspace, workspace_bytes);
+    if (st != KVC8_OK) return st;
+    if (launch_plan(q, context_lengths, context_seq_offset, nullptr, workspace, dev_error,
+                    stream) != cudaSuccess)
+        return KVC8_ERR_CUDA;
+    GatherBf16Args a;
+    a.g = q;
+    a.k_cache = static_cast<const uint16_t *>(key_cache);
+    a.v_cache = static_cast<const uint16_t *>(value_cache);
+    a.block_table = block_table;
+    a.context_lengths = context_lengths;
+    a.k_out = static_cast<uint16_t *>(key_out);
+    a.v_out = static_cast<uint16_t *>(value_out);
+    a.out_rows = out_rows;
+    a.out_tok_stride = out_tok_stride;
+    a.out_head_stride = out_head_stride;
+    a.plan = workspace;
+    a.dev_error = dev_error;
+    return cuda_status(launch_gather_bf16(a, /*use_pdl=*/true, stream));
+}
+
 kvc8_status kvc8_get_error(int32_t *dev_error, int32_t *host_code, int32_t reset,
                            cudaStream_t stream) {
     if (dev_error == nullptr || host_code == nullptr) return KVC8_ERR_INVALID_ARG;

@@ -72,6 +72,24 @@ __device__ __forceinline__ void report(int32_t *dev_error, int32_t code) {
     if (dev_error != nullptr) atomicCAS(dev_error, 0, code);
 }
 
+// Sequence of a new token (shared by the int8 and bf16 stores).
+// Largest b in [0, B] with cu[b] <= t (cu[0] = 0 <= t < cu[B]), found by the
+// whole warp: each round samples 32 evenly spaced entries of the current range
+// at once and keeps the last sample <= t, so the range shrinks 32-fold per
+// round (two rounds for a thousand sequences).  All lanes get the same answer.
+__device__ __forceinline__ int seq_of_token(const int32_t *cu, int B, int64_t t, int lane) {
+    int lo = 0, hi = B;  // cu[lo] <= t < cu[hi]
+    while (hi - lo > 1) {
+        const int step = (hi - lo + 31) >> 5;
+        const int idx = lo + step * (lane + 1);
+        const bool le = idx < hi && (int64_t)ld_nc_s32(cu + idx) <= t;
+        const unsigned m = __ballot_sync(0xFFFFFFFFu, le);
+        if (m != 0u) lo += step * (32 - __clz(m));
+        hi = min(hi, lo + step);
+    }
+    return lo;
+}
+
 // ---------------------------------------------------------------------------
 // Gather plan, written by the plan kernel into the caller's workspace.
 //   header.total_tiles : number of (sequence, logical block) tiles
@@ -134,7 +152,40 @@ struct GatherArgs {
     int32_t *dev_error;
 };
 
+// bf16 paged cache (no quantisation): caches are uint16_t (bf16 bits).
+struct StoreBf16Args {
+    kvc8_geom g;
+    int64_t num_tokens;
+    const uint16_t *k_states;
+    const uint16_t *v_states;
+    int64_t x_tok_stride;
+    int64_t x_head_stride;
+    uint16_t *k_cache;
+    uint16_t *v_cache;
+    const int32_t *block_table;
+    const int32_t *cu_q_lens;
+    const int32_t *context_kv_lens;
+    int32_t *dev_error;
+};
+
+struct GatherBf16Args {
+    kvc8_geom g;
+    const uint16_t *k_cache;
+    const uint16_t *v_cache;
+    const int32_t *block_table;
+    const int32_t *context_lengths;
+    uint16_t *k_out;
+    uint16_t *v_out;
+    int64_t out_rows;
+    int64_t out_tok_stride;
+    int64_t out_head_stride;
+    const void *plan;
+    int32_t *dev_error;
+};
+
 cudaError_t launch_store(const StoreArgs &a, cudaStream_t stream);
+cudaError_t launch_store_bf16(const StoreBf16Args &a, cudaStream_t stream);
+cudaError_t launch_gather_bf16(const GatherBf16Args &a, bool use_pdl, cudaStream_t stream);
 cudaError_t launch_plan(const kvc8_geom &g, const int32_t *context_lengths,
                         const int64_t *context_seq_offset, int64_t *offsets_out, void *plan,
                         int32_t *dev_error, cudaStream_t stream);

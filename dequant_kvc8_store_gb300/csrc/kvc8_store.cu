@@ -74,23 +74,6 @@ __device__ __forceinline__ uint32_t pack_lo_bytes(uint32_t a, uint32_t b, uint32
     return __byte_perm(__byte_perm(a, b, 0x0040), __byte_perm(c, d, 0x0040), 0x5410);
 }
 
-// Largest b in [0, B] with cu[b] <= t (cu[0] = 0 <= t < cu[B]), found by the
-// whole warp: each round samples 32 evenly spaced entries of the current range
-// at once and keeps the last sample <= t, so the range shrinks 32-fold per
-// round (two rounds for a thousand sequences).  All lanes get the same answer.
-__device__ __forceinline__ int seq_of_token(const int32_t *cu, int B, int64_t t, int lane) {
-    int lo = 0, hi = B;  // cu[lo] <= t < cu[hi]
-    while (hi - lo > 1) {
-        const int step = (hi - lo + 31) >> 5;
-        const int idx = lo + step * (lane + 1);
-        const bool le = idx < hi && (int64_t)ld_nc_s32(cu + idx) <= t;
-        const unsigned m = __ballot_sync(0xFFFFFFFFu, le);
-        if (m != 0u) lo += step * (32 - __clz(m));
-        hi = min(hi, lo + step);
-    }
-    return lo;
-}
-
 template <bool V32>
 __device__ __forceinline__ void load32(const uint16_t *p, uint32_t w[8]) {
     if (V32) {

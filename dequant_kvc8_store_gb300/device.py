@@ -116,3 +116,55 @@ class DeviceBatch:
 
     def host_outputs(self):
         return bf16_bits(self.k_out), bf16_bits(self.v_out)
+
+
+class Bf16Batch:
+    """Holds a Workload's tokens, metadata and a bf16 page pool [NB][H][bs][D]
+    (no quantisation) on the GPU, for kvc8_store_bf16 / kvc8_gather_bf16.  The
+    pool starts as seeded random bits; outputs are dense [rows][H][D]."""
+
+    def __init__(self, w: Workload, device="cuda", seed=0):
+        self.w = w
+        dev = self.device = torch.device(device)
+        self.g = B.Geom(w.num_seqs, w.kv_heads, w.head_dim, w.block_size, w.num_blocks,
+                        w.max_blocks_per_seq, 0)
+        H, D = w.kv_heads, w.head_dim
+        self.k_states = self.v_states = None
+        if w.has_store:
+            self.k_states = _bf16(w.k_states).to(dev)
+            self.v_states = _bf16(w.v_states).to(dev)
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(seed)
+        shape = (w.num_blocks, H, w.block_size, D)
+        self.k_cache = torch.randint(-32768, 32768, shape, dtype=torch.int16, device=dev,
+                                     generator=gen).view(torch.bfloat16)
+        self.v_cache = torch.randint(-32768, 32768, shape, dtype=torch.int16, device=dev,
+                                     generator=gen).view(torch.bfloat16)
+        self.block_table = torch.from_numpy(w.block_table).to(dev)
+        self.cu_q_lens = None if w.cu_q_lens is None else torch.from_numpy(w.cu_q_lens).to(dev)
+        self.context_kv_lens = torch.from_numpy(w.context_kv_lens).to(dev)
+        self.context_lengths = torch.from_numpy(w.context_lengths).to(dev)
+        self.out_rows = w.total_context
+        self.k_out = torch.empty((self.out_rows, H, D), dtype=torch.bfloat16, device=dev)
+        self.v_out = torch.empty((self.out_rows, H, D), dtype=torch.bfloat16, device=dev)
+        self.ws_bytes = B.kvc8_gather_workspace_bytes(self.g)
+        self.workspace = torch.empty(max(self.ws_bytes, 256), dtype=torch.uint8, device=dev)
+        self.dev_error = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def store(self, stream=None):
+        if self.k_states is None:
+            return
+        ks = self.k_states
+        B.kvc8_store_bf16(self.g, ks.shape[0], ks, self.v_states, ks.stride(0), ks.stride(1),
+                          self.k_cache, self.v_cache, self.block_table, self.cu_q_lens,
+                          self.context_kv_lens, self.dev_error, stream)
+
+    def gather(self, stream=None):
+        ko = self.k_out
+        B.kvc8_gather_bf16(self.g, self.k_cache, self.v_cache, self.block_table,
+                           self.context_lengths, None, ko, self.v_out, self.out_rows,
+                           ko.stride(0), ko.stride(1), self.workspace, self.ws_bytes,
+                           self.dev_error, stream)
+
+    def error_code(self, reset=False) -> int:
+        return B.kvc8_get_error(self.dev_error, reset=reset)

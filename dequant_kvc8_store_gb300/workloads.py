@@ -297,3 +297,11 @@ def algorithmic_bytes(w: Workload) -> dict:
     store = rows_store * (2 * D + D + per_row_scale) + (table if w.num_tokens else 0)
     gather = rows_gather * (D + per_row_scale + 2 * D) + (table if w.total_context else 0)
     return {"store": int(store), "gather": int(gather)}
+
+
+def algorithmic_bytes_bf16(w: Workload) -> dict:
+    """Algorithmic HBM bytes of one store and one gather of the bf16 cache (no
+    quantisation): every row is read once and written once, 2*D bytes each way."""
+    H, D = w.kv_heads, w.head_dim
+    return {"store": int(2 * H * w.num_tokens * 4 * D),
+            "gather": int(2 * H * w.total_context * 4 * D)}

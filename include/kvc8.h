@@ -236,6 +236,39 @@ kvc8_status kvc8_dequant_gather_planned(const kvc8_geom *g, const int8_t *key_ca
                                         void *workspace, size_t workspace_bytes,
                                         int32_t *dev_error, cudaStream_t stream);
 
+/*
+ * kvc8_store_bf16 -- the same scatter as kvc8_store for a bf16 paged cache,
+ * without quantisation: MojoStorePagedKVCache of the "Mojo Opset" README
+ * ("Op List", KVCache), the int8 store's sibling ([PR379] pass 1, "Must fix":
+ * the sibling checks cu_q_lens; here a NULL cu_q_lens means decode, as in
+ * kvc8_store).  Each new token's K and V rows are copied bit for bit to
+ * key_cache/value_cache[block][h][slot][0:D] (bf16 [NB][H][bs][D]), with the
+ * slot mapping and the argument and error conventions of kvc8_store;
+ * g->quant_mode is ignored.
+ */
+kvc8_status kvc8_store_bf16(const kvc8_geom *g, int64_t num_tokens,
+                            const void *key_states, const void *value_states,
+                            int64_t x_tok_stride, int64_t x_head_stride,
+                            void *key_cache, void *value_cache,
+                            const int32_t *block_table, const int32_t *cu_q_lens,
+                            const int32_t *context_kv_lens, int32_t *dev_error,
+                            cudaStream_t stream);
+
+/*
+ * kvc8_gather_bf16 -- gather a bf16 paged cache into contiguous rows (the
+ * layout of kvc8_dequant_gather's output, values copied bit for bit), with the
+ * plan, offsets, strides, workspace and error conventions of
+ * kvc8_dequant_gather; g->quant_mode is ignored.
+ */
+kvc8_status kvc8_gather_bf16(const kvc8_geom *g, const void *key_cache,
+                             const void *value_cache, const int32_t *block_table,
+                             const int32_t *context_lengths,
+                             const int64_t *context_seq_offset, void *key_out,
+                             void *value_out, int64_t out_rows, int64_t out_tok_stride,
+                             int64_t out_head_stride, void *workspace,
+                             size_t workspace_bytes, int32_t *dev_error,
+                             cudaStream_t stream);
+
 /* Largest num_seqs that kvc8_dequant_gather_noalloc accepts. */
 #define KVC8_NOALLOC_MAX_SEQS 4096
 

@@ -115,6 +115,11 @@ class Oracle:
         lib.orc_round_to_bf16.restype = ctypes.c_uint16
         lib.orc_row_scale_bf16.argtypes = [P, i32]
         lib.orc_row_scale_bf16.restype = ctypes.c_float
+        lib.orc_store_bf16.argtypes = [i32, i64, i32, i32, i32, i32, i32, P, P, P, P, P, P, P]
+        lib.orc_store_bf16.restype = i32
+        lib.orc_gather_bf16.argtypes = [i32, i32, i32, i32, i32, i32, P, P, P, P, P, P, P,
+                                        i64, i64, i64]
+        lib.orc_gather_bf16.restype = i32
         self.lib = lib
         self.path = lib_path
 
@@ -227,6 +232,41 @@ class Oracle:
                "orc_dequant_positions")
         return k_rows, v_rows
 
+    def store_bf16(self, k_bits, v_bits, k_cache, v_cache, block_table, cu_q_lens,
+                   context_kv_lens):
+        """bf16 store (no quantisation) into uint16 caches [NB][H][bs][D], in place."""
+        for a in (k_cache, v_cache):
+            if not a.flags.c_contiguous or a.dtype != np.uint16:
+                raise ValueError("caches must be C-contiguous uint16")
+        k, v = _c(k_bits, np.uint16), _c(v_bits, np.uint16)
+        bt = _c(block_table, np.int32)
+        cu = _c(cu_q_lens, np.int32)
+        ctx = _c(context_kv_lens, np.int32)
+        NB, H, bs, D = k_cache.shape
+        B, MB = bt.shape
+        _check(self.lib.orc_store_bf16(B, k.shape[0], H, D, bs, NB, MB, _ptr(k), _ptr(v),
+                                       _ptr(k_cache), _ptr(v_cache), _ptr(bt), _ptr(cu),
+                                       _ptr(ctx)), "orc_store_bf16")
+
+    def gather_bf16(self, k_cache, v_cache, block_table, context_lengths,
+                    context_seq_offset=None, k_out=None, v_out=None, out_rows=None):
+        """Gather of a bf16 cache; returns (k_out, v_out) uint16 [rows][H][D]."""
+        kc, vc = _c(k_cache, np.uint16), _c(v_cache, np.uint16)
+        bt = _c(block_table, np.int32)
+        ctx = _c(context_lengths, np.int32)
+        off = _c(context_seq_offset, np.int64)
+        NB, H, bs, D = kc.shape
+        B, MB = bt.shape
+        if k_out is None:
+            rows = int(out_rows if out_rows is not None else int(ctx.astype(np.int64).sum()))
+            k_out = np.zeros((rows, H, D), np.uint16)
+            v_out = np.zeros((rows, H, D), np.uint16)
+        rows = k_out.shape[0]
+        _check(self.lib.orc_gather_bf16(B, H, D, bs, NB, MB, _ptr(kc), _ptr(vc), _ptr(bt),
+                                        _ptr(ctx), _ptr(off), _ptr(k_out), _ptr(v_out), rows,
+                                        H * D, D), "orc_gather_bf16")
+        return k_out, v_out
+
     def slots(self, block_table, block_size, num_blocks, seq, pos):
         """Physical (block, slot) arrays for (seq, pos) pairs; -1 where out of range."""
         bt = _c(block_table, np.int32)
@@ -257,6 +297,6 @@ def __getattr__(name):
     # module-level shortcuts: oracle.store(...), oracle.dequant_gather(...), ...
     if name in {"quantize_value", "dequantize_value", "round_to_bf16", "row_scale",
                 "quantize_rows", "store", "exclusive_cumsum", "dequant_gather",
-                "dequant_positions", "slots"}:
+                "dequant_positions", "slots", "store_bf16", "gather_bf16"}:
         return getattr(default(), name)
     raise AttributeError(name)

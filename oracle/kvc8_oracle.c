@@ -364,3 +364,79 @@ float orc_row_scale_bf16(const uint16_t *row, int head_dim)
 {
     return orc_row_scale(row, head_dim);
 }
+
+/* ---- bf16 paged cache without quantisation ---------------------------------
+ * MojoStorePagedKVCache, the int8 store's sibling ("Mojo Opset" README, "Op
+ * List"; [PR379] pass 1, "Must fix", on the cu_q_lens check it performs): the
+ * same placement as orc_store, with each row copied as is.  Caches are bf16
+ * bits [num_blocks][H][block_size][D]. */
+int orc_store_bf16(int num_seqs, int64_t num_tokens, int kv_heads, int head_dim,
+                   int block_size, int num_blocks, int max_blocks_per_seq,
+                   const uint16_t *k_states, const uint16_t *v_states,
+                   uint16_t *k_cache, uint16_t *v_cache,
+                   const int32_t *block_table, const int32_t *cu_q_lens,
+                   const int32_t *context_kv_lens)
+{
+    const int64_t row_elems = (int64_t)kv_heads * head_dim;
+    for (int b = 0; b < num_seqs; ++b) {
+        int64_t first = cu_q_lens ? cu_q_lens[b] : b;
+        int64_t count = cu_q_lens ? (int64_t)cu_q_lens[b + 1] - cu_q_lens[b] : 1;
+        if (count < 0 || first < 0 || first + count > num_tokens)
+            return ORC_ERR_BOUNDS;
+        for (int64_t i = 0; i < count; ++i) {
+            int32_t blk, slot;
+            int rc = orc_slot(block_table, max_blocks_per_seq, block_size,
+                              num_blocks, b, (int64_t)context_kv_lens[b] + i,
+                              &blk, &slot);
+            if (rc != ORC_OK)
+                return rc;
+            for (int kv = 0; kv < 2; ++kv) {
+                const uint16_t *xs = kv ? v_states : k_states;
+                uint16_t *cache = kv ? v_cache : k_cache;
+                for (int h = 0; h < kv_heads; ++h) {
+                    const uint16_t *src = xs + (first + i) * row_elems + (int64_t)h * head_dim;
+                    uint16_t *dst = cache + (((int64_t)blk * kv_heads + h) * block_size + slot) * head_dim;
+                    for (int d = 0; d < head_dim; ++d)
+                        dst[d] = src[d];
+                }
+            }
+        }
+    }
+    return ORC_OK;
+}
+
+/* Gather of the bf16 cache: the layout and offsets of orc_dequant_gather,
+ * values copied as is. */
+int orc_gather_bf16(int num_seqs, int kv_heads, int head_dim, int block_size,
+                    int num_blocks, int max_blocks_per_seq, const uint16_t *k_cache,
+                    const uint16_t *v_cache, const int32_t *block_table,
+                    const int32_t *context_lengths, const int64_t *context_seq_offset,
+                    uint16_t *k_out, uint16_t *v_out, int64_t out_rows,
+                    int64_t tok_stride, int64_t head_stride)
+{
+    int64_t acc = 0;
+    for (int b = 0; b < num_seqs; ++b) {
+        int64_t off = context_seq_offset ? context_seq_offset[b] : acc;
+        acc += context_lengths[b];
+        for (int64_t p = 0; p < context_lengths[b]; ++p) {
+            int32_t blk, slot;
+            int rc = orc_slot(block_table, max_blocks_per_seq, block_size,
+                              num_blocks, b, p, &blk, &slot);
+            if (rc != ORC_OK)
+                return rc;
+            if (off + p < 0 || off + p >= out_rows)
+                return ORC_ERR_BOUNDS;
+            for (int kv = 0; kv < 2; ++kv) {
+                const uint16_t *cache = kv ? v_cache : k_cache;
+                uint16_t *out = kv ? v_out : k_out;
+                for (int h = 0; h < kv_heads; ++h) {
+                    const uint16_t *src = cache + (((int64_t)blk * kv_heads + h) * block_size + slot) * head_dim;
+                    uint16_t *dst = out + (off + p) * tok_stride + (int64_t)h * head_stride;
+                    for (int d = 0; d < head_dim; ++d)
+                        dst[d] = src[d];
+                }
+            }
+        }
+    }
+    return ORC_OK;
+}

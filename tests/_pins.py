@@ -347,6 +347,84 @@ def pin_bounds_errors(orc):
         raise AssertionError("out-of-range store accepted")
 
 
+# ---- bf16 cache (no quantisation) -----------------------------------------------
+
+def pin_bf16_placement_golden(orc):
+    """The hand-worked placement of tests/golden/placement_tiny.txt, with a bf16
+    cache: rows land, and are gathered, bit for bit."""
+    g = _golden.placement()
+    H, D = 1, 16
+    bs, NB = g["block_size"], g["num_blocks"]
+    n_tok = int(g["cu_q_lens"][-1])
+    x = _token_rows_placement(n_tok, D)
+    y = x ^ np.uint16(0x0001)  # V rows differ from K rows
+    kc = np.full((NB, H, bs, D), 0x1234, np.uint16)
+    vc = np.full((NB, H, bs, D), 0x4321, np.uint16)
+    orc.store_bf16(x, y, kc, vc, g["block_table"], g["cu_q_lens"], g["context_kv_lens"])
+    owner = {v: t for t, v in g["expect_slot"].items()}
+    for blk in range(NB):
+        for slot in range(bs):
+            t = owner.get((blk, slot))
+            want_k = x[t, 0] if t is not None else np.full(D, 0x1234, np.uint16)
+            want_v = y[t, 0] if t is not None else np.full(D, 0x4321, np.uint16)
+            assert np.array_equal(kc[blk, 0, slot], want_k), (blk, slot)
+            assert np.array_equal(vc[blk, 0, slot], want_v), (blk, slot)
+    for gg in g["gathers"]:
+        rows = gg.get("out_rows", len(gg["rows"]))
+        ko = np.full((rows, H, D), 0xFFFF, np.uint16)
+        vo = np.full((rows, H, D), 0xFFFF, np.uint16)
+        orc.gather_bf16(kc, vc, g["block_table"], gg["context_lengths"], gg.get("offsets"), ko, vo)
+        for r, tag in enumerate(gg["rows"]):
+            if tag == "F":
+                wk = wv = np.full(D, 0xFFFF, np.uint16)
+            elif tag == "S":
+                wk, wv = np.full(D, 0x1234, np.uint16), np.full(D, 0x4321, np.uint16)
+            else:
+                wk, wv = x[int(tag), 0], y[int(tag), 0]
+            assert np.array_equal(ko[r, 0], wk) and np.array_equal(vo[r, 0], wv), (r, tag)
+
+
+def pin_bf16_bruteforce(orc):
+    """Random tiny problems against a dict model of logical -> physical rows."""
+    rng = np.random.default_rng(777)
+    for it in range(16):
+        B = int(rng.integers(1, 5)); H = int(rng.integers(1, 3)); D = 16
+        bs = int(rng.choice([1, 2, 4, 16])); MB = int(rng.integers(1, 5))
+        NB = B * MB + int(rng.integers(0, 3)); cap = MB * bs
+        ctx = rng.integers(0, cap + 1, size=B)
+        q = np.array([rng.integers(0, cap - c + 1) for c in ctx])
+        bt = rng.permutation(NB).astype(np.int32)[:B * MB].reshape(B, MB).copy()
+        N = int(q.sum())
+        x = rng.integers(0, 1 << 16, size=(N, H, D)).astype(np.uint16)
+        y = rng.integers(0, 1 << 16, size=(N, H, D)).astype(np.uint16)
+        kc = rng.integers(0, 1 << 16, size=(NB, H, bs, D)).astype(np.uint16)
+        vc = rng.integers(0, 1 << 16, size=(NB, H, bs, D)).astype(np.uint16)
+        kc0, vc0 = kc.copy(), vc.copy()
+        cu = np.concatenate([[0], np.cumsum(q)]).astype(np.int32)
+        orc.store_bf16(x, y, kc, vc, bt, cu, ctx.astype(np.int32))
+        logical = {}
+        tok = 0
+        for b in range(B):
+            for i in range(int(q[b])):
+                logical[(b, int(ctx[b]) + i)] = tok
+                tok += 1
+        phys = {(int(bt[b][p // bs]), p % bs): t for (b, p), t in logical.items()}
+        for blk in range(NB):
+            for slot in range(bs):
+                t = phys.get((blk, slot))
+                assert np.array_equal(kc[blk, :, slot], kc0[blk, :, slot] if t is None else x[t])
+                assert np.array_equal(vc[blk, :, slot], vc0[blk, :, slot] if t is None else y[t])
+        lens = (ctx + q).astype(np.int32)
+        ko, vo = orc.gather_bf16(kc, vc, bt, lens)
+        row = 0
+        for b in range(B):
+            for p in range(int(lens[b])):
+                blk, slot = int(bt[b][p // bs]), p % bs
+                assert np.array_equal(ko[row], kc[blk, :, slot]) and np.array_equal(vo[row], vc[blk, :, slot])
+                row += 1
+
+
 PINS = [pin_quantize_goldens, pin_dequant_goldens, pin_placement_golden,
         pin_exact_quantize_random, pin_exact_dequant_random, pin_invariants,
-        pin_identity_table, pin_cumsum, pin_placement_bruteforce, pin_bounds_errors]
+        pin_identity_table, pin_cumsum, pin_placement_bruteforce, pin_bounds_errors,
+        pin_bf16_placement_golden, pin_bf16_bruteforce]

@@ -132,3 +132,43 @@ def test_build_metadata_rejects_bad_arguments():
 def test_get_error_rejects_null():
     code = ctypes.c_int32()
     assert kv.load().kvc8_get_error(None, ctypes.byref(code), 0, None) == kv.ERR_INVALID_ARG
+
+
+def _store_bf16(g, n=4, **kw):
+    a = dict(ks=FAKE, vs=FAKE, ts=g.kv_heads * g.head_dim, hs=g.head_dim, kc=FAKE, vc=FAKE,
+             bt=FAKE, cu=FAKE, ctx=FAKE)
+    a.update(kw)
+    return kv.load().kvc8_store_bf16(ctypes.byref(g), n, a["ks"], a["vs"], a["ts"], a["hs"],
+                                     a["kc"], a["vc"], a["bt"], a["cu"], a["ctx"], None, None)
+
+
+def _gather_bf16(g, **kw):
+    a = dict(kc=FAKE, vc=FAKE, bt=FAKE, lens=FAKE, off=None, ko=FAKE, vo=FAKE, rows=10,
+             ts=g.kv_heads * g.head_dim, hs=g.head_dim, ws=FAKE, wsb=1 << 20)
+    a.update(kw)
+    return kv.load().kvc8_gather_bf16(ctypes.byref(g), a["kc"], a["vc"], a["bt"], a["lens"],
+                                      a["off"], a["ko"], a["vo"], a["rows"], a["ts"], a["hs"],
+                                      a["ws"], a["wsb"], None, None)
+
+
+def test_bf16_store_and_gather_reject_bad_arguments():
+    g = kv.Geom(2, 8, 128, 16, 64, 8, 0)
+    for name in ("ks", "vs", "kc", "vc", "bt", "ctx"):
+        assert _store_bf16(g, **{name: None}) == kv.ERR_INVALID_ARG, name
+    assert _store_bf16(g, ts=1028) == kv.ERR_INVALID_ARG
+    assert _store_bf16(g, kc=FAKE + 2) == kv.ERR_INVALID_ARG
+    assert _store_bf16(g, n=3, cu=None) == kv.ERR_INVALID_ARG
+    assert _store_bf16(g, n=-1) == kv.ERR_INVALID_ARG
+    assert _store_bf16(g, n=1 << 31) == kv.ERR_UNSUPPORTED
+    assert _store_bf16(g, n=0, ks=None) == kv.OK
+    # the quantisation mode is not used: any value is accepted
+    assert _store_bf16(kv.Geom(2, 8, 128, 16, 64, 8, 7), n=0) == kv.OK
+    assert _store_bf16(kv.Geom(2, 8, 24, 16, 64, 8, 0)) == kv.ERR_INVALID_ARG
+    for name in ("kc", "vc", "bt", "lens", "ko", "vo"):
+        assert _gather_bf16(g, **{name: None}) == kv.ERR_INVALID_ARG, name
+    assert _gather_bf16(g, rows=-1) == kv.ERR_INVALID_ARG
+    assert _gather_bf16(g, hs=4) == kv.ERR_INVALID_ARG
+    assert _gather_bf16(g, vo=FAKE + 8) == kv.ERR_INVALID_ARG
+    assert _gather_bf16(g, ws=None) == kv.ERR_WORKSPACE
+    assert _gather_bf16(g, wsb=16) == kv.ERR_WORKSPACE
+    assert _gather_bf16(kv.Geom(0, 8, 128, 16, 64, 8, 0), kc=None) == kv.OK

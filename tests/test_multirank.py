@@ -53,7 +53,7 @@ def _rank_main(rank, world, port, out):
 def test_two_gloo_ranks_agree_on_the_slowest_step():
     world = 2
     port = _free_port()
-    with mp.Manager() as mgr:
+    with mp.get_context("spawn").Manager() as mgr:
         out = mgr.dict()
         mp.start_processes(_rank_main, args=(world, port, out), nprocs=world, join=True,
                            start_method="spawn")

@@ -38,6 +38,10 @@ MUTATIONS = [
     ("dequant_scale_squared", [("float prod = (float)q * s;", "float prod = (float)q * s * s;")]),
     ("absmax_without_abs", [("float a = fabsf(orc_bf16_to_f32(row[d]));",
                              "float a = orc_bf16_to_f32(row[d]);")]),
+    ("bf16_store_drops_context", [("num_blocks, b, (int64_t)context_kv_lens[b] + i,",
+                                   "num_blocks, b, (int64_t)i,")]),
+    ("bf16_gather_heads_swapped", [("uint16_t *dst = out + (off + p) * tok_stride + (int64_t)h * head_stride;\n                    for (int d = 0; d < head_dim; ++d)\n                        dst[d] = src[d];",
+                                    "uint16_t *dst = out + (off + p) * tok_stride + (int64_t)(kv_heads - 1 - h) * head_stride;\n                    for (int d = 0; d < head_dim; ++d)\n                        dst[d] = src[d];")]),
 ]
 
 
