@@ -146,7 +146,7 @@ def test_bf16_strided_inputs_and_outputs():
 
 def test_bf16_side_stream_and_gather_only():
     w = W.make_workload("bf16side", q_lens=[0, 0, 0], ctx_before=[129, 1, 640], kv_heads=8,
-                        head_dim=128, block_size=64, num_blocks=20, quant_mode=0, seed=171,
+                        head_dim=128, block_size=64, num_blocks=30, quant_mode=0, seed=171,
                         with_store=False)
     s = torch.cuda.Stream()
     with torch.cuda.stream(s):
