@@ -52,6 +52,8 @@ KERNEL_SOURCES = ["dequant_kvc8_store_gb300/csrc/kvc8_store.cu",
                   "dequant_kvc8_store_gb300/csrc/kvc8_gather.cu",
                   "dequant_kvc8_store_gb300/csrc/kvc8_bf16.cu",
                   "dequant_kvc8_store_gb300/csrc/kvc8_internal.cuh"]
+PATH_TEXT = {"c8": "int8 cache", "bf16": "bf16 cache, no quantisation",
+             "fused": "int8 cache, store and gather fused into one append + gather launch"}
 WORKLOAD_TEXT = {
     "tiny": "tiny round trip: batch 2, q {5,19} after {3,0} cached, 2 kv heads x 64, block 16, "
             "8 blocks, dynamic scales",
@@ -222,15 +224,21 @@ def run_gpu(args, rank, world):
 
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
 
+    fused = args.path == "fused"
+
     def step(e=None):
-        flush_l2(1)
+        if not fused:
+            flush_l2(1)
         if e: e[0].record(stream)
-        if has_store:
+        if has_store and not fused:
             d.store(stream)
         if e: e[1].record(stream)
         flush_l2(2)
         if e: e[2].record(stream)
-        d.gather(stream)  # plan kernel + gather kernel (programmatic dependent launch)
+        if fused:
+            d.append_gather(stream)  # plan kernel + fused append/gather kernel
+        else:
+            d.gather(stream)  # plan kernel + gather kernel (programmatic dependent launch)
         if e: e[3].record(stream)
 
     for _ in range(args.warmup):
@@ -249,7 +257,7 @@ def run_gpu(args, rank, world):
             step(ev[i])
         barrier()
         wall = time.perf_counter() - t0
-    st_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    st_ms = [0.0 if fused else e[0].elapsed_time(e[1]) for e in ev]
     ga_ms = [e[2].elapsed_time(e[3]) for e in ev]
     step_ms = [a + b for a, b in zip(st_ms, ga_ms)]
     if d.error_code() != 0:
@@ -289,8 +297,11 @@ def run_e2e(args, w, d, dev, nbytes):
     def step():
         for name, t in host.items():
             getattr(d, name).copy_(t, non_blocking=True)
-        d.store(stream)
-        d.gather(stream)
+        if args.path == "fused":
+            d.append_gather(stream)
+        else:
+            d.store(stream)
+            d.gather(stream)
         out_k.copy_(d.k_out, non_blocking=True)
         out_v.copy_(d.v_out, non_blocking=True)
 
@@ -373,7 +384,11 @@ def oracle_pass(w: W.Workload, path: str = "c8"):
 
 
 def path_bytes(w: W.Workload, path: str) -> dict:
-    return W.algorithmic_bytes_bf16(w) if path == "bf16" else W.algorithmic_bytes(w)
+    if path == "bf16":
+        return W.algorithmic_bytes_bf16(w)
+    if path == "fused":
+        return W.algorithmic_bytes_fused(w)
+    return W.algorithmic_bytes(w)
 
 
 def cpu_baseline(w: W.Workload, path: str = "c8", seconds: float = 12.0,
@@ -425,7 +440,7 @@ def run_reference(args, rank, world):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if args.path == "bf16" else "f32",
         "data": "synthetic", "config": {"workload": WORKLOAD_TEXT[args.workload],
-                                        "path": "bf16 cache, no quantisation" if args.path == "bf16" else "int8 cache",
+                                        "path": PATH_TEXT[args.path],
                                         "sample_positions_per_step": int(s.q_lens().sum() + s.context_lengths.astype(np.int64).sum())},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": f"each step: oracle store+gather of the first {s.num_seqs} "
@@ -445,8 +460,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["kvc8", "reference"], default="kvc8")
     ap.add_argument("--workload", choices=list(W.NAMED), default="prefill")
-    ap.add_argument("--path", choices=["c8", "bf16"], default="c8",
-                    help="c8: the int8 cache (default); bf16: the cache without quantisation")
+    ap.add_argument("--path", choices=["c8", "bf16", "fused"], default="c8",
+                    help="c8: the int8 cache (default); bf16: the cache without quantisation; "
+                         "fused: the int8 store and gather as one append + gather pass")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -465,16 +481,23 @@ def main():
         peak, peak_kind = measured_peak()
         total = nbytes["store"] + nbytes["gather"]
         value = job_throughput(total, world, t["step_ms"])
+        fused = args.path == "fused"
         ops = {
             "store": {"ms": round(t["store_ms"], 5),
                       "GB_s": round(nbytes["store"] / (t["store_ms"] * 1e-3) / 1e9, 1) if has_store else None,
                       "tokens_per_s": round(w.num_tokens / (t["store_ms"] * 1e-3), 1) if has_store else None,
                       "bytes": nbytes["store"]},
-            "dequant_gather": {"ms": round(t["gather_ms"], 5), "kernels": "plan + gather",
+            "dequant_gather": {"ms": round(t["gather_ms"], 5),
+                               "kernels": "plan + fused append/gather" if fused else "plan + gather",
                                "GB_s": round(nbytes["gather"] / (t["gather_ms"] * 1e-3) / 1e9, 1),
                                "tokens_per_s": round(w.total_context / (t["gather_ms"] * 1e-3), 1),
                                "bytes": nbytes["gather"]},
         }
+        if fused:  # one op: the store is inside the fused launch
+            ops["store"] = {"ms": 0.0, "GB_s": None, "tokens_per_s": None, "bytes": 0,
+                            "note": "done inside the fused append + gather launch"}
+            ops["dequant_gather"]["appended_tokens_per_s"] = round(
+                w.num_tokens / (t["gather_ms"] * 1e-3), 1) if has_store else None
         # the dominant kernel: the op with the larger device time
         dom = "dequant_gather" if (t["gather_ms"] >= t["store_ms"] or not has_store) else "store"
         dom_bytes = nbytes["gather"] if dom == "dequant_gather" else nbytes["store"]
@@ -483,6 +506,8 @@ def main():
         kname = "gather" if dom == "dequant_gather" else "store"
         if args.path == "bf16":
             kname += "_bf16"
+        if fused:
+            kname = "append_gather"
         traffic = ncu_traffic(args.workload).get(kname + "_kernel")
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
@@ -491,7 +516,7 @@ def main():
             "dtype": "bf16" if args.path == "bf16" else "f32",
             "data": "synthetic",
             "config": {"workload": WORKLOAD_TEXT[args.workload],
-                       "path": "bf16 cache, no quantisation" if args.path == "bf16" else "int8 cache",
+                       "path": PATH_TEXT[args.path],
                        "l2": "flushed before each timed op (256 MiB write, then 256 MiB read)",
                        "hbm_frac_of_step": round(total / (t["step_ms"] * 1e-3) / 1e9 / peak, 4),
                        "tokens_per_s": {"store": ops["store"]["tokens_per_s"],
@@ -501,7 +526,7 @@ def main():
                          "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                          "peak_kind": peak_kind, "traffic": traffic,
                          "algorithmic_bytes": dom_bytes},
-            "gpu_launches": args.steps * (3 if has_store else 2),
+            "gpu_launches": args.steps * (3 if has_store and not fused else 2),
             "clocks": clocks,
             "e2e": e2e,
             "wall_s": round(t["wall_s"], 3),

@@ -86,6 +86,14 @@ def configure(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.kvc8_store_bf16.restype = ctypes.c_int
     lib.kvc8_gather_bf16.argtypes = [G, P, P, P, P, P, P, P, i64, i64, i64, P, sz, P, P]
     lib.kvc8_gather_bf16.restype = ctypes.c_int
+    lib.kvc8_append_gather.argtypes = [G, i64, P, P, i64, i64, P, P, P, P, P, P, P, P, P, P, i64,
+                                       i64, i64, P, sz, P, P]
+    lib.kvc8_append_gather.restype = ctypes.c_int
+    lib.kvc8_build_append_metadata.argtypes = [G, P, P, P, P, P, sz, P, P]
+    lib.kvc8_build_append_metadata.restype = ctypes.c_int
+    lib.kvc8_append_gather_planned.argtypes = [G, i64, P, P, i64, i64, P, P, P, P, P, P, P, P, P,
+                                               i64, i64, i64, P, sz, P, P]
+    lib.kvc8_append_gather_planned.restype = ctypes.c_int
     return lib
 
 
@@ -230,6 +238,43 @@ def kvc8_gather_bf16(g: Geom, key_cache, value_cache, block_table, context_lengt
                                  int(out_head_stride), _p(workspace), int(workspace_bytes),
                                  _p(dev_error), _stream(stream))
     _ok(st, "kvc8_gather_bf16")
+
+
+def kvc8_append_gather(g: Geom, num_tokens, key_states, value_states, x_tok_stride,
+                       x_head_stride, key_cache, value_cache, key_scale, value_scale, block_table,
+                       cu_q_lens, context_kv_lens, context_seq_offset, key_out, value_out,
+                       out_rows, out_tok_stride, out_head_stride, workspace, workspace_bytes,
+                       dev_error=None, stream=None) -> None:
+    st = load().kvc8_append_gather(
+        ctypes.byref(g), int(num_tokens), _p(key_states), _p(value_states), int(x_tok_stride),
+        int(x_head_stride), _p(key_cache), _p(value_cache), _p(key_scale), _p(value_scale),
+        _p(block_table), _p(cu_q_lens), _p(context_kv_lens), _p(context_seq_offset),
+        _p(key_out), _p(value_out), int(out_rows), int(out_tok_stride), int(out_head_stride),
+        _p(workspace), int(workspace_bytes), _p(dev_error), _stream(stream))
+    _ok(st, "kvc8_append_gather")
+
+
+def kvc8_build_append_metadata(g: Geom, cu_q_lens, context_kv_lens, context_seq_offset,
+                               offsets_out, workspace, workspace_bytes, dev_error=None,
+                               stream=None) -> None:
+    st = load().kvc8_build_append_metadata(
+        ctypes.byref(g), _p(cu_q_lens), _p(context_kv_lens), _p(context_seq_offset),
+        _p(offsets_out), _p(workspace), int(workspace_bytes), _p(dev_error), _stream(stream))
+    _ok(st, "kvc8_build_append_metadata")
+
+
+def kvc8_append_gather_planned(g: Geom, num_tokens, key_states, value_states, x_tok_stride,
+                               x_head_stride, key_cache, value_cache, key_scale, value_scale,
+                               block_table, cu_q_lens, context_kv_lens, key_out, value_out,
+                               out_rows, out_tok_stride, out_head_stride, workspace,
+                               workspace_bytes, dev_error=None, stream=None) -> None:
+    st = load().kvc8_append_gather_planned(
+        ctypes.byref(g), int(num_tokens), _p(key_states), _p(value_states), int(x_tok_stride),
+        int(x_head_stride), _p(key_cache), _p(value_cache), _p(key_scale), _p(value_scale),
+        _p(block_table), _p(cu_q_lens), _p(context_kv_lens), _p(key_out), _p(value_out),
+        int(out_rows), int(out_tok_stride), int(out_head_stride), _p(workspace),
+        int(workspace_bytes), _p(dev_error), _stream(stream))
+    _ok(st, "kvc8_append_gather_planned")
 
 
 def kvc8_get_error(dev_error, reset: bool = False, stream=None) -> int:

@@ -219,6 +219,129 @@ kvc8_status kvc8_dequant_gather_planned(const kvc8_geom *g, const int8_t *key_ca
     return cuda_status(launch_gather(a, /*use_pdl=*/false, stream));
 }
 
+// Shared checks and argument packing of the append + gather entry points.
+static kvc8_status append_args(const kvc8_geom *g, int64_t num_tokens, const void *key_states,
+                               const void *value_states, int64_t x_tok_stride,
+                               int64_t x_head_stride, int8_t *key_cache, int8_t *value_cache,
+                               float *key_scale, float *value_scale,
+                               const int32_t *block_table, const int32_t *cu_q_lens,
+                               const int32_t *context_kv_lens, void *key_out, void *value_out,
+                               int64_t out_rows, int64_t out_tok_stride,
+                               int64_t out_head_stride, void *workspace,
+                               size_t workspace_bytes, int32_t *dev_error, GatherArgs *a,
+                               AppendArgs *p) {
+    kvc8_status st = check_geom(g);
+    if (st != KVC8_OK) return st;
+    if (num_tokens < 0) return KVC8_ERR_INVALID_ARG;
+    if (num_tokens > INT32_MAX) return KVC8_ERR_UNSUPPORTED;  // token indices are 32-bit
+    if (cu_q_lens == nullptr && num_tokens != g->num_seqs) return KVC8_ERR_INVALID_ARG;
+    st = check_gather_args(g, key_cache, value_cache, key_scale, value_scale, block_table,
+                           context_kv_lens, key_out, value_out, out_rows, out_tok_stride,
+                           out_head_stride);
+    if (st != KVC8_OK) return st;
+    if (num_tokens > 0) {
+        if (key_states == nullptr || value_states == nullptr) return KVC8_ERR_INVALID_ARG;
+        if (x_tok_stride < 0 || x_head_stride < 0 || x_tok_stride % 8 != 0 ||
+            x_head_stride % 8 != 0)
+            return KVC8_ERR_INVALID_ARG;
+        if (!aligned(key_states, 16) || !aligned(value_states, 16)) return KVC8_ERR_INVALID_ARG;
+    }
+    st = check_workspace(g, workspace, workspace_bytes);
+    if (st != KVC8_OK) return st;
+    a->g = *g;
+    a->k_cache = key_cache;
+    a->v_cache = value_cache;
+    a->k_scale = key_scale;
+    a->v_scale = value_scale;
+    a->block_table = block_table;
+    a->context_lengths = context_kv_lens;  // the gather part reads the cached positions
+    a->k_out = static_cast<uint16_t *>(key_out);
+    a->v_out = static_cast<uint16_t *>(value_out);
+    a->out_rows = out_rows;
+    a->out_tok_stride = out_tok_stride;
+    a->out_head_stride = out_head_stride;
+    a->plan = workspace;
+    a->dev_error = dev_error;
+    p->num_tokens = num_tokens;
+    const int64_t rows = num_tokens * 2 * g->kv_heads;
+    p->items = (rows + kAppendRowsPerItem - 1) / kAppendRowsPerItem;
+    p->k_states = static_cast<const uint16_t *>(key_states);
+    p->v_states = static_cast<const uint16_t *>(value_states);
+    p->x_tok_stride = x_tok_stride;
+    p->x_head_stride = x_head_stride;
+    p->k_cache = key_cache;
+    p->v_cache = value_cache;
+    p->k_scale = key_scale;
+    p->v_scale = value_scale;
+    p->cu_q_lens = cu_q_lens;
+    p->context_kv_lens = context_kv_lens;
+    return KVC8_OK;
+}
+
+kvc8_status kvc8_append_gather(const kvc8_geom *g, int64_t num_tokens, const void *key_states,
+                               const void *value_states, int64_t x_tok_stride,
+                               int64_t x_head_stride, int8_t *key_cache, int8_t *value_cache,
+                               float *key_scale, float *value_scale,
+                               const int32_t *block_table, const int32_t *cu_q_lens,
+                               const int32_t *context_kv_lens,
+                               const int64_t *context_seq_offset, void *key_out,
+                               void *value_out, int64_t out_rows, int64_t out_tok_stride,
+                               int64_t out_head_stride, void *workspace,
+                               size_t workspace_bytes, int32_t *dev_error, cudaStream_t stream) {
+    if (g != nullptr && g->num_seqs == 0 && check_geom(g) == KVC8_OK)
+        return num_tokens == 0 ? KVC8_OK : KVC8_ERR_INVALID_ARG;
+    GatherArgs a;
+    AppendArgs p;
+    kvc8_status st = append_args(g, num_tokens, key_states, value_states, x_tok_stride,
+                                 x_head_stride, key_cache, value_cache, key_scale, value_scale,
+                                 block_table, cu_q_lens, context_kv_lens, key_out, value_out,
+                                 out_rows, out_tok_stride, out_head_stride, workspace,
+                                 workspace_bytes, dev_error, &a, &p);
+    if (st != KVC8_OK) return st;
+    if (launch_plan_append(*g, context_kv_lens, cu_q_lens, context_seq_offset, nullptr,
+                           workspace, dev_error, stream) != cudaSuccess)
+        return KVC8_ERR_CUDA;
+    return cuda_status(launch_append_gather(a, p, /*use_pdl=*/true, stream));
+}
+
+kvc8_status kvc8_build_append_metadata(const kvc8_geom *g, const int32_t *cu_q_lens,
+                                       const int32_t *context_kv_lens,
+                                       const int64_t *context_seq_offset, int64_t *offsets_out,
+                                       void *workspace, size_t workspace_bytes,
+                                       int32_t *dev_error, cudaStream_t stream) {
+    kvc8_status st = check_geom(g);
+    if (st != KVC8_OK) return st;
+    if (context_kv_lens == nullptr && g->num_seqs > 0) return KVC8_ERR_INVALID_ARG;
+    st = check_workspace(g, workspace, workspace_bytes);
+    if (st != KVC8_OK) return st;
+    return cuda_status(launch_plan_append(*g, context_kv_lens, cu_q_lens, context_seq_offset,
+                                          offsets_out, workspace, dev_error, stream));
+}
+
+kvc8_status kvc8_append_gather_planned(const kvc8_geom *g, int64_t num_tokens,
+                                       const void *key_states, const void *value_states,
+                                       int64_t x_tok_stride, int64_t x_head_stride,
+                                       int8_t *key_cache, int8_t *value_cache, float *key_scale,
+                                       float *value_scale, const int32_t *block_table,
+                                       const int32_t *cu_q_lens, const int32_t *context_kv_lens,
+                                       void *key_out, void *value_out, int64_t out_rows,
+                                       int64_t out_tok_stride, int64_t out_head_stride,
+                                       void *workspace, size_t workspace_bytes,
+                                       int32_t *dev_error, cudaStream_t stream) {
+    if (g != nullptr && g->num_seqs == 0 && check_geom(g) == KVC8_OK)
+        return num_tokens == 0 ? KVC8_OK : KVC8_ERR_INVALID_ARG;
+    GatherArgs a;
+    AppendArgs p;
+    kvc8_status st = append_args(g, num_tokens, key_states, value_states, x_tok_stride,
+                                 x_head_stride, key_cache, value_cache, key_scale, value_scale,
+                                 block_table, cu_q_lens, context_kv_lens, key_out, value_out,
+                                 out_rows, out_tok_stride, out_head_stride, workspace,
+                                 workspace_bytes, dev_error, &a, &p);
+    if (st != KVC8_OK) return st;
+    if (reset_plan_counter(workspace, stream) != cudaSuccess) return KVC8_ERR_CUDA;
+    return cuda_status(launch_append_gather(a, p, /*use_pdl=*/false, stream));
+}
+
 // Geometry checks for the bf16 cache (quant_mode is not used there).
 static kvc8_status check_geom_bf16(const kvc8_geom *g) {
     if (g == nullptr) return KVC8_ERR_INVALID_ARG;

@@ -62,7 +62,11 @@ __device__ T block_inclusive_scan(T v, T *warp_tot) {
 __global__ void __launch_bounds__(kPlanThreads)
 plan_kernel(const kvc8_geom g, const int32_t *__restrict__ lens,
             const int64_t *__restrict__ given_off, int64_t *__restrict__ offsets_out,
-            char *__restrict__ plan, int32_t *__restrict__ dev_error) {
+            char *__restrict__ plan, int32_t *__restrict__ dev_error,
+            const int32_t *__restrict__ cu_q, int q_mode) {
+    // lens: the positions gathered from the cache per sequence.  q_mode 0:
+    // the output rows of a sequence are exactly those; 1: an append adds
+    // cu_q[b+1] - cu_q[b] rows after them; 2: an append adds one row.
     // The gather may start launching now; it waits for this grid to finish
     // (griddepcontrol.wait) before it reads the plan.
     pdl_launch_dependents();
@@ -80,7 +84,7 @@ plan_kernel(const kvc8_geom g, const int32_t *__restrict__ lens,
     __syncthreads();
     for (int base = 0; base < B; base += kPlanThreads) {
         const int i = base + threadIdx.x;
-        int64_t len = 0;
+        int64_t len = 0, span = 0;  // span: output rows of the sequence
         int32_t tiles = 0;
         if (i < B) {
             len = lens[i];
@@ -88,6 +92,17 @@ plan_kernel(const kvc8_geom g, const int32_t *__restrict__ lens,
                 report(dev_error, KVC8_DEV_BAD_LENGTH);
                 len = 0;
             }
+            int64_t q = 0;
+            if (q_mode == 1) {
+                q = (int64_t)cu_q[i + 1] - cu_q[i];
+                if (q < 0) {
+                    report(dev_error, KVC8_DEV_BAD_LENGTH);
+                    q = 0;
+                }
+            } else if (q_mode == 2) {
+                q = 1;
+            }
+            span = len + q;
             int64_t t64 = (len + bs - 1) / bs;
             if (t64 > MB) {
                 report(dev_error, KVC8_DEV_POS_BEYOND_TABLE);
@@ -97,10 +112,10 @@ plan_kernel(const kvc8_geom g, const int32_t *__restrict__ lens,
         }
         const int64_t carry_len = carry_len_s;
         const int32_t carry_tiles = carry_tiles_s;
-        const int64_t inc_len = block_inclusive_scan<int64_t>(len, tot64);
+        const int64_t inc_len = block_inclusive_scan<int64_t>(span, tot64);
         const int32_t inc_tiles = block_inclusive_scan<int32_t>(tiles, tot32);
         if (i < B) {
-            const int64_t o = given_off != nullptr ? given_off[i] : carry_len + inc_len - len;
+            const int64_t o = given_off != nullptr ? given_off[i] : carry_len + inc_len - span;
             off[i] = o;
             ts[i] = carry_tiles + inc_tiles - tiles;
             if (offsets_out != nullptr) offsets_out[i] = o;
@@ -193,12 +208,127 @@ __device__ __forceinline__ void store_chunk(uint16_t *p, const uint32_t *o) {
     }
 }
 
+// Append part of the fused append + gather: row r = (token t, K|V, head h) of
+// the new tokens, one per warp.  Lane l holds values [8l, 8l + 8) of the row.
+// The codes follow the definition directly -- s = fl(amax / 127) (mode 0) or
+// the static scale, q = clamp(rne(fl(x / s)), -127, 127), 0 when s = 0 --
+// because an append is a handful of rows per sequence and its time is latency.
+// The output values are formed exactly as the gather forms them from the
+// cache: fl(float(q) * s), rounded to bf16 (RNE).
+template <int MODE, int CH>
+__device__ __forceinline__ void append_row(const GatherArgs &a, const AppendArgs &p, int64_t r,
+                                           const int64_t *off, const float *s_tab) {
+    const int H = a.g.kv_heads, D = a.g.head_dim, bs = a.g.block_size;
+    const int B = a.g.num_seqs, MB = a.g.max_blocks_per_seq, NB = a.g.num_blocks;
+    const int lane = threadIdx.x & 31;
+    if (r >= p.num_tokens * 2 * H) return;  // warp-uniform
+    const int64_t t = r / (2 * H);
+    const int u = (int)(r - t * 2 * H);
+    const int kv = u >= H, h = u - kv * H;
+    const bool on = lane < (D >> 3);
+    uint4 x = make_uint4(0u, 0u, 0u, 0u);
+    if (on)
+        x = ld_stream_16((kv ? p.v_states : p.k_states) + t * p.x_tok_stride +
+                         (int64_t)h * p.x_head_stride + lane * 8);
+
+    // slot of token t (warp-uniform)
+    int b;
+    int64_t i_in_seq;
+    bool bad_len = false;
+    if (p.cu_q_lens != nullptr) {
+        b = seq_of_token(p.cu_q_lens, B, t, lane);
+        const int64_t first = ld_nc_s32(p.cu_q_lens + b);
+        const int64_t next = ld_nc_s32(p.cu_q_lens + b + 1);
+        i_in_seq = t - first;
+        bad_len = !(first <= t && t < next);
+    } else {
+        b = (int)t;
+        i_in_seq = 0;
+    }
+    const int64_t ctx = ld_nc_s32(p.context_kv_lens + b);
+    const int64_t pos = ctx + i_in_seq;
+    const int64_t lb = pos / bs;
+    int32_t err = 0, blk = 0;
+    if (bad_len || ctx < 0) {
+        err = KVC8_DEV_BAD_LENGTH;
+    } else if (lb >= MB) {
+        err = KVC8_DEV_POS_BEYOND_TABLE;
+    } else {
+        blk = ld_nc_s32(a.block_table + (int64_t)b * MB + lb);
+        if (blk < 0 || blk >= NB) err = KVC8_DEV_BAD_BLOCK_ID;
+    }
+    if (err != 0) {
+        if (lane == 0) report(a.dev_error, err);
+        return;
+    }
+    const int64_t slot = pos - lb * bs;
+
+    const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
+    float v[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        v[2 * k] = __uint_as_float(xw[k] << 16);
+        v[2 * k + 1] = __uint_as_float(xw[k] & 0xFFFF0000u);
+    }
+    float sc[8];
+    if (MODE == 0) {
+        float m = 0.0f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(v[e]));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+        const float s = __fdiv_rn(m, 127.0f);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) sc[e] = s;
+    } else {
+        constexpr int SPAD = CH + 4;
+        const int CPR = D / CH;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const int d = on ? lane * 8 + e : 0;
+            sc[e] = s_tab[((kv * H + h) * CPR + d / CH) * SPAD + d % CH];
+        }
+    }
+    int q[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+        q[e] = sc[e] == 0.0f ? 0 : min(127, max(-127, __float2int_rn(__fdiv_rn(v[e], sc[e]))));
+
+    const int64_t row = ((int64_t)blk * H + h) * bs + slot;
+    if (on) {
+        const uint32_t c0 = __byte_perm(__byte_perm((uint32_t)q[0], (uint32_t)q[1], 0x0040),
+                                        __byte_perm((uint32_t)q[2], (uint32_t)q[3], 0x0040), 0x5410);
+        const uint32_t c1 = __byte_perm(__byte_perm((uint32_t)q[4], (uint32_t)q[5], 0x0040),
+                                        __byte_perm((uint32_t)q[6], (uint32_t)q[7], 0x0040), 0x5410);
+        st_8((kv ? p.v_cache : p.k_cache) + row * D + lane * 8, c0, c1);
+    }
+    if (MODE == 0 && lane == 0) (kv ? p.v_scale : p.k_scale)[row] = sc[0];
+
+    const int64_t orow = off[b] + pos;
+    if (orow < 0 || orow >= a.out_rows) {
+        if (lane == 0) report(a.dev_error, KVC8_DEV_OUT_ROW_RANGE);
+        return;
+    }
+    if (on) {
+        uint32_t o[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            o[k] = bf16x2_rn(__fmul_rn((float)q[2 * k], sc[2 * k]),
+                             __fmul_rn((float)q[2 * k + 1], sc[2 * k + 1]));
+        st_stream_16((kv ? a.v_out : a.k_out) + orow * a.out_tok_stride +
+                         (int64_t)h * a.out_head_stride + lane * 8,
+                     o[0], o[1], o[2], o[3]);
+    }
+}
+
 // A work item is one tile (sequence b, logical block j) and a pair of (K|V,
 // head) slabs: units 2r and 2r+1 of the tile's 2H units, so both slabs share
 // the tile's metadata.  Items are handed out by an atomic counter in the plan.
-template <int MODE, int CH, bool WIDE>
+// APPEND: the fused append + gather; items [0, p.items) are append items
+// (kAppendRowsPerItem rows each), the gather items follow.
+template <int MODE, int CH, bool WIDE, bool APPEND>
 __global__ void __launch_bounds__(kGatherThreads)
-gather_kernel(const GatherArgs a) {
+gather_kernel(const GatherArgs a, const AppendArgs p) {
     constexpr int W = CH / 4;  // words per chunk
     constexpr int PER = 1;     // chunks per slab per thread per round
     const int H = a.g.kv_heads, D = a.g.head_dim, bs = a.g.block_size;
@@ -226,15 +356,24 @@ gather_kernel(const GatherArgs a) {
     const int32_t *ts = reinterpret_cast<const int32_t *>(plan + plan_tile_start_at(B));
     unsigned long long *counter =
         reinterpret_cast<unsigned long long *>(const_cast<int64_t *>(&hdr->work_counter));
-    const int64_t items = hdr->total_tiles * H;
+    const int64_t items = hdr->total_tiles * H + (APPEND ? p.items : 0);
 
     int64_t item = blockIdx.x;
     while (item < items) {
         long long next = 0;
         if (threadIdx.x == 0) next = (long long)atomicAdd(counter, 1ull) + gridDim.x;
+        if (APPEND && item < p.items) {
+            append_row<MODE, CH>(a, p, item * kAppendRowsPerItem + (threadIdx.x >> 5), off, s_tab);
+            if (threadIdx.x == 0) s_item = next;
+            __syncthreads();
+            item = s_item;
+            __syncthreads();
+            continue;
+        }
+        const int64_t gitem = APPEND ? item - p.items : item;
 
-        const int64_t tile = item / H;
-        const int r2 = (int)(item - tile * H);
+        const int64_t tile = gitem / H;
+        const int r2 = (int)(gitem - tile * H);
         const int b = seq_of_tile(ts, B, tile);
         const int64_t j = tile - ts[b];
         const int64_t len = ld_nc_s32(a.context_lengths + b);
@@ -305,9 +444,10 @@ gather_kernel(const GatherArgs a) {
     }
 }
 
-template <int MODE, int CH, bool WIDE>
-cudaError_t launch_gather_variant(const GatherArgs &a, bool use_pdl, cudaStream_t stream) {
-    auto kern = gather_kernel<MODE, CH, WIDE>;
+template <int MODE, int CH, bool WIDE, bool APPEND>
+cudaError_t launch_gather_variant(const GatherArgs &a, const AppendArgs &p, bool use_pdl,
+                                  cudaStream_t stream) {
+    auto kern = gather_kernel<MODE, CH, WIDE, APPEND>;
     const size_t smem = MODE == 1 ? sizeof(float) * 2 * a.g.kv_heads * (a.g.head_dim / CH) * (CH + 4) : 0;
     static int cached_dev = -1;
     static size_t cached_smem = 0;
@@ -330,7 +470,8 @@ cudaError_t launch_gather_variant(const GatherArgs &a, bool use_pdl, cudaStream_
         cached_smem = smem;
         cached_dev = dev;
     }
-    const int64_t max_items = (int64_t)a.g.num_seqs * a.g.max_blocks_per_seq * a.g.kv_heads;
+    const int64_t max_items = (int64_t)a.g.num_seqs * a.g.max_blocks_per_seq * a.g.kv_heads +
+                              (APPEND ? p.items : 0);
     const int64_t cap = (int64_t)sm_count() * occ;
     const int grid = (int)(max_items < cap ? max_items : cap);
     if (grid <= 0) return cudaSuccess;
@@ -344,13 +485,29 @@ cudaError_t launch_gather_variant(const GatherArgs &a, bool use_pdl, cudaStream_
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = use_pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, kern, a);
+    return cudaLaunchKernelEx(&cfg, kern, a, p);
 }
 
-template <int MODE, bool WIDE>
-cudaError_t launch_gather_mode(const GatherArgs &a, bool use_pdl, cudaStream_t stream) {
-    if (a.g.head_dim % 32 == 0) return launch_gather_variant<MODE, 32, WIDE>(a, use_pdl, stream);
-    return launch_gather_variant<MODE, 16, WIDE>(a, use_pdl, stream);
+template <int MODE, bool WIDE, bool APPEND>
+cudaError_t launch_gather_mode(const GatherArgs &a, const AppendArgs &p, bool use_pdl,
+                               cudaStream_t stream) {
+    if (a.g.head_dim % 32 == 0)
+        return launch_gather_variant<MODE, 32, WIDE, APPEND>(a, p, use_pdl, stream);
+    return launch_gather_variant<MODE, 16, WIDE, APPEND>(a, p, use_pdl, stream);
+}
+
+template <bool APPEND>
+cudaError_t launch_gather_any(const GatherArgs &a, const AppendArgs &p, bool use_pdl,
+                              cudaStream_t stream) {
+    const uintptr_t k = reinterpret_cast<uintptr_t>(a.k_out);
+    const uintptr_t v = reinterpret_cast<uintptr_t>(a.v_out);
+    const bool wide = (k % 32 == 0) && (v % 32 == 0) && (a.out_tok_stride % 16 == 0) &&
+                      (a.out_head_stride % 16 == 0);
+    if (a.g.quant_mode == 0)
+        return wide ? launch_gather_mode<0, true, APPEND>(a, p, use_pdl, stream)
+                    : launch_gather_mode<0, false, APPEND>(a, p, use_pdl, stream);
+    return wide ? launch_gather_mode<1, true, APPEND>(a, p, use_pdl, stream)
+                : launch_gather_mode<1, false, APPEND>(a, p, use_pdl, stream);
 }
 
 }  // namespace
@@ -359,7 +516,18 @@ cudaError_t launch_plan(const kvc8_geom &g, const int32_t *context_lengths,
                         const int64_t *context_seq_offset, int64_t *offsets_out, void *plan,
                         int32_t *dev_error, cudaStream_t stream) {
     plan_kernel<<<1, kPlanThreads, 0, stream>>>(g, context_lengths, context_seq_offset,
-                                                offsets_out, static_cast<char *>(plan), dev_error);
+                                                offsets_out, static_cast<char *>(plan), dev_error,
+                                                nullptr, 0);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_plan_append(const kvc8_geom &g, const int32_t *context_kv_lens,
+                               const int32_t *cu_q_lens, const int64_t *context_seq_offset,
+                               int64_t *offsets_out, void *plan, int32_t *dev_error,
+                               cudaStream_t stream) {
+    plan_kernel<<<1, kPlanThreads, 0, stream>>>(g, context_kv_lens, context_seq_offset,
+                                                offsets_out, static_cast<char *>(plan), dev_error,
+                                                cu_q_lens, cu_q_lens != nullptr ? 1 : 2);
     return cudaGetLastError();
 }
 
@@ -369,15 +537,12 @@ cudaError_t reset_plan_counter(void *plan, cudaStream_t stream) {
 }
 
 cudaError_t launch_gather(const GatherArgs &a, bool use_pdl, cudaStream_t stream) {
-    const uintptr_t k = reinterpret_cast<uintptr_t>(a.k_out);
-    const uintptr_t v = reinterpret_cast<uintptr_t>(a.v_out);
-    const bool wide = (k % 32 == 0) && (v % 32 == 0) && (a.out_tok_stride % 16 == 0) &&
-                      (a.out_head_stride % 16 == 0);
-    if (a.g.quant_mode == 0)
-        return wide ? launch_gather_mode<0, true>(a, use_pdl, stream)
-                    : launch_gather_mode<0, false>(a, use_pdl, stream);
-    return wide ? launch_gather_mode<1, true>(a, use_pdl, stream)
-                : launch_gather_mode<1, false>(a, use_pdl, stream);
+    return launch_gather_any<false>(a, AppendArgs{}, use_pdl, stream);
+}
+
+cudaError_t launch_append_gather(const GatherArgs &a, const AppendArgs &p, bool use_pdl,
+                                 cudaStream_t stream) {
+    return launch_gather_any<true>(a, p, use_pdl, stream);
 }
 
 }  // namespace kvc8

@@ -183,12 +183,44 @@ struct GatherBf16Args {
     int32_t *dev_error;
 };
 
+// Fused append + gather: the new tokens' rows, quantised and written to the
+// cache, and their dequantised values written straight to the output rows
+// after each sequence's cached positions.  The gather part of the same launch
+// reads only the cached positions (GatherArgs.context_lengths = the cached
+// lengths), so the two parts touch disjoint cache bytes.
+struct AppendArgs {
+    int64_t num_tokens;
+    int64_t items;  // append work items (kAppendRowsPerItem rows each), first in the item order
+    const uint16_t *k_states;
+    const uint16_t *v_states;
+    int64_t x_tok_stride;
+    int64_t x_head_stride;
+    int8_t *k_cache;
+    int8_t *v_cache;
+    float *k_scale;  // mode 0: the scale caches (written); mode 1: the static scales
+    float *v_scale;
+    const int32_t *cu_q_lens;  // NULL: one new token per sequence
+    const int32_t *context_kv_lens;
+};
+
+constexpr int kAppendRowsPerItem = 8;  // one (token, K|V, head) row per warp of a CTA
+
 cudaError_t launch_store(const StoreArgs &a, cudaStream_t stream);
 cudaError_t launch_store_bf16(const StoreBf16Args &a, cudaStream_t stream);
 cudaError_t launch_gather_bf16(const GatherBf16Args &a, bool use_pdl, cudaStream_t stream);
 cudaError_t launch_plan(const kvc8_geom &g, const int32_t *context_lengths,
                         const int64_t *context_seq_offset, int64_t *offsets_out, void *plan,
                         int32_t *dev_error, cudaStream_t stream);
+// Plan of an append + gather: tiles cover the cached lengths, offsets the
+// lengths after the append (cached + new tokens, new = cu_q_lens[b+1] -
+// cu_q_lens[b], or 1 each when cu_q_lens is NULL).
+cudaError_t launch_plan_append(const kvc8_geom &g, const int32_t *context_kv_lens,
+                               const int32_t *cu_q_lens, const int64_t *context_seq_offset,
+                               int64_t *offsets_out, void *plan, int32_t *dev_error,
+                               cudaStream_t stream);
+// The fused append + gather launch (a programmatic dependent of the plan when use_pdl).
+cudaError_t launch_append_gather(const GatherArgs &a, const AppendArgs &p, bool use_pdl,
+                                 cudaStream_t stream);
 // use_pdl: launch as a programmatic dependent of the previous kernel (the plan).
 cudaError_t launch_gather(const GatherArgs &a, bool use_pdl, cudaStream_t stream);
 // Zero the gather's work counter in a plan built earlier (for planned gathers).

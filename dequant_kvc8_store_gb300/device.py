@@ -105,6 +105,39 @@ class DeviceBatch:
                                       self.v_out, self.out_rows, ko.stride(0), ko.stride(1),
                                       self.workspace, self.ws_bytes, self.dev_error, stream)
 
+    def _append_operands(self):
+        ks = self.k_states
+        if ks is None:  # nothing to append: every sequence gets zero new tokens
+            if getattr(self, "_zero_cu", None) is None:
+                self._zero_cu = torch.zeros(self.w.num_seqs + 1, dtype=torch.int32,
+                                            device=self.device)
+            return 0, None, None, 0, 0, self._zero_cu
+        return ks.shape[0], ks, self.v_states, ks.stride(0), ks.stride(1), self.cu_q_lens
+
+    def append_gather(self, stream=None):
+        """The store and the gather of the whole context in one pass (plan +
+        one fused launch)."""
+        n, ks, vs, ts, hs, cu = self._append_operands()
+        ko = self.k_out
+        B.kvc8_append_gather(self.g, n, ks, vs, ts, hs, self.k_cache, self.v_cache, self.k_scale,
+                             self.v_scale, self.block_table, cu, self.context_kv_lens,
+                             self.offsets, ko, self.v_out, self.out_rows, ko.stride(0),
+                             ko.stride(1), self.workspace, self.ws_bytes, self.dev_error, stream)
+
+    def build_append_metadata(self, offsets_out=None, stream=None):
+        _, _, _, _, _, cu = self._append_operands()
+        B.kvc8_build_append_metadata(self.g, cu, self.context_kv_lens, self.offsets, offsets_out,
+                                     self.workspace, self.ws_bytes, self.dev_error, stream)
+
+    def append_gather_planned(self, stream=None):
+        n, ks, vs, ts, hs, cu = self._append_operands()
+        ko = self.k_out
+        B.kvc8_append_gather_planned(self.g, n, ks, vs, ts, hs, self.k_cache, self.v_cache,
+                                     self.k_scale, self.v_scale, self.block_table, cu,
+                                     self.context_kv_lens, ko, self.v_out, self.out_rows,
+                                     ko.stride(0), ko.stride(1), self.workspace, self.ws_bytes,
+                                     self.dev_error, stream)
+
     def error_code(self, reset=False) -> int:
         return B.kvc8_get_error(self.dev_error, reset=reset)
 

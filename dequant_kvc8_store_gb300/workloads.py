@@ -305,3 +305,17 @@ def algorithmic_bytes_bf16(w: Workload) -> dict:
     H, D = w.kv_heads, w.head_dim
     return {"store": int(2 * H * w.num_tokens * 4 * D),
             "gather": int(2 * H * w.total_context * 4 * D)}
+
+
+def algorithmic_bytes_fused(w: Workload) -> dict:
+    """Algorithmic HBM bytes of one fused append + gather (K and V together):
+    the store's bytes for the new tokens, the gather's bytes for the cached
+    positions, and the bf16 output rows of the new tokens (written once, never
+    read back from the cache)."""
+    H, D = w.kv_heads, w.head_dim
+    table = 2 * H * D * 4 if w.quant_mode == 1 else 0
+    per_row_scale = 4 if w.quant_mode == 0 else 0
+    cached = 2 * H * int(w.context_kv_lens.astype(np.int64).sum())
+    new = 2 * H * w.num_tokens
+    total = new * (2 * D + D + per_row_scale + 2 * D) + cached * (D + per_row_scale + 2 * D)
+    return {"store": 0, "gather": int(total + table)}

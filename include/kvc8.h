@@ -237,6 +237,73 @@ kvc8_status kvc8_dequant_gather_planned(const kvc8_geom *g, const int8_t *key_ca
                                         int32_t *dev_error, cudaStream_t stream);
 
 /*
+ * kvc8_append_gather -- kvc8_store followed by kvc8_dequant_gather of every
+ * sequence's whole context (cached + new tokens), in one pass over the data.
+ * The pages run these as two ops on the decode path (MojoStorePagedKVCacheC8
+ * with cu_q_lens NULL "in decode", [PR379] pass 2 "Must fix"; then
+ * MojoDequantFromPagedKVCache, every pass "Must fix").  The result is
+ * bit-identical to the two calls with context_lengths[b] = context_kv_lens[b]
+ * + q_b (q_b = cu_q_lens[b+1] - cu_q_lens[b], or 1 when cu_q_lens is NULL):
+ * the same codes and scales land in the cache and the same bf16 rows in the
+ * output.  The new tokens' rows are quantised once; their codes and scales go
+ * to the cache and their dequantised values straight to output rows
+ * offset_b + context_kv_lens[b] + i, while the same launch gathers the cached
+ * positions [0, context_kv_lens[b]) from the cache.  Enqueues a plan (into
+ * `workspace`) and one fused launch that overlaps the plan's tail.
+ *
+ * Arguments: the new tokens, strides, caches, scales, block table, cu_q_lens
+ * and context_kv_lens as in kvc8_store (num_tokens == cu_q_lens[B]); the
+ * offsets, outputs, strides, workspace and error word as in
+ * kvc8_dequant_gather, where context_seq_offset (or, when NULL, the exclusive
+ * prefix sum of context_kv_lens + q) places each sequence.  num_tokens == 0
+ * is a plain gather of the cached positions.  Errors as in the two calls; an
+ * output row outside [0, out_rows) is reported and not written (its codes are
+ * still stored).
+ */
+kvc8_status kvc8_append_gather(const kvc8_geom *g, int64_t num_tokens, const void *key_states,
+                               const void *value_states, int64_t x_tok_stride,
+                               int64_t x_head_stride, int8_t *key_cache, int8_t *value_cache,
+                               float *key_scale, float *value_scale,
+                               const int32_t *block_table, const int32_t *cu_q_lens,
+                               const int32_t *context_kv_lens,
+                               const int64_t *context_seq_offset, void *key_out,
+                               void *value_out, int64_t out_rows, int64_t out_tok_stride,
+                               int64_t out_head_stride, void *workspace,
+                               size_t workspace_bytes, int32_t *dev_error, cudaStream_t stream);
+
+/*
+ * kvc8_build_append_metadata -- the plan of kvc8_append_gather alone, written
+ * into `workspace` (same size rule as kvc8_build_metadata): tiles over the
+ * cached positions context_kv_lens[b], offsets over context_kv_lens[b] + q_b
+ * (or the caller's context_seq_offset), optionally copied to offsets_out.
+ * Lets the layers of one model step share one plan through
+ * kvc8_append_gather_planned.
+ */
+kvc8_status kvc8_build_append_metadata(const kvc8_geom *g, const int32_t *cu_q_lens,
+                                       const int32_t *context_kv_lens,
+                                       const int64_t *context_seq_offset, int64_t *offsets_out,
+                                       void *workspace, size_t workspace_bytes,
+                                       int32_t *dev_error, cudaStream_t stream);
+
+/*
+ * kvc8_append_gather_planned -- kvc8_append_gather with a plan that an earlier
+ * kvc8_build_append_metadata wrote into `workspace` for the same cu_q_lens,
+ * context_kv_lens, offsets and geometry.  One fused launch (after an 8-byte
+ * memset of the plan's work counter; calls that overlap on the GPU need
+ * separate workspaces).  Arguments as in kvc8_append_gather.
+ */
+kvc8_status kvc8_append_gather_planned(const kvc8_geom *g, int64_t num_tokens,
+                                       const void *key_states, const void *value_states,
+                                       int64_t x_tok_stride, int64_t x_head_stride,
+                                       int8_t *key_cache, int8_t *value_cache, float *key_scale,
+                                       float *value_scale, const int32_t *block_table,
+                                       const int32_t *cu_q_lens, const int32_t *context_kv_lens,
+                                       void *key_out, void *value_out, int64_t out_rows,
+                                       int64_t out_tok_stride, int64_t out_head_stride,
+                                       void *workspace, size_t workspace_bytes,
+                                       int32_t *dev_error, cudaStream_t stream);
+
+/*
  * kvc8_store_bf16 -- the same scatter as kvc8_store for a bf16 paged cache,
  * without quantisation: MojoStorePagedKVCache of the "Mojo Opset" README
  * ("Op List", KVCache), the int8 store's sibling ([PR379] pass 1, "Must fix":

@@ -172,3 +172,46 @@ def test_bf16_store_and_gather_reject_bad_arguments():
     assert _gather_bf16(g, ws=None) == kv.ERR_WORKSPACE
     assert _gather_bf16(g, wsb=16) == kv.ERR_WORKSPACE
     assert _gather_bf16(kv.Geom(0, 8, 128, 16, 64, 8, 0), kc=None) == kv.OK
+
+
+def _append(g, fn="kvc8_append_gather", n=2, **kw):
+    a = dict(ks=FAKE, vs=FAKE, ts=g.kv_heads * g.head_dim, hs=g.head_dim, kc=FAKE, vc=FAKE,
+             ksc=FAKE, vsc=FAKE, bt=FAKE, cu=FAKE, ctx=FAKE, off=None, ko=FAKE, vo=FAKE, rows=10,
+             ots=g.kv_heads * g.head_dim, ohs=g.head_dim, ws=FAKE, wsb=1 << 20)
+    a.update(kw)
+    lib = kv.load()
+    head = [ctypes.byref(g), n, a["ks"], a["vs"], a["ts"], a["hs"], a["kc"], a["vc"], a["ksc"],
+            a["vsc"], a["bt"], a["cu"], a["ctx"]]
+    tail = [a["ko"], a["vo"], a["rows"], a["ots"], a["ohs"], a["ws"], a["wsb"], None, None]
+    if fn == "kvc8_append_gather":
+        return lib.kvc8_append_gather(*head, a["off"], *tail)
+    return lib.kvc8_append_gather_planned(*head, *tail)
+
+
+@pytest.mark.parametrize("fn", ["kvc8_append_gather", "kvc8_append_gather_planned"])
+def test_append_gather_rejects_bad_arguments(fn):
+    g = kv.Geom(2, 8, 128, 16, 64, 8, 0)
+    for name in ("ks", "vs", "kc", "vc", "ksc", "vsc", "bt", "ctx", "ko", "vo"):
+        assert _append(g, fn, **{name: None}) == kv.ERR_INVALID_ARG, name
+    assert _append(g, fn, ts=1028) == kv.ERR_INVALID_ARG
+    assert _append(g, fn, ks=FAKE + 2) == kv.ERR_INVALID_ARG
+    assert _append(g, fn, ohs=4) == kv.ERR_INVALID_ARG
+    assert _append(g, fn, rows=-1) == kv.ERR_INVALID_ARG
+    assert _append(g, fn, n=3, cu=None) == kv.ERR_INVALID_ARG  # decode form: one per sequence
+    assert _append(g, fn, n=-1) == kv.ERR_INVALID_ARG
+    assert _append(g, fn, n=1 << 31) == kv.ERR_UNSUPPORTED
+    assert _append(g, fn, ws=None) == kv.ERR_WORKSPACE
+    assert _append(g, fn, wsb=16) == kv.ERR_WORKSPACE
+    assert _append(kv.Geom(2, 8, 128, 16, 64, 8, 3), fn) == kv.ERR_INVALID_ARG
+    g0 = kv.Geom(0, 8, 128, 16, 64, 8, 0)
+    assert _append(g0, fn, n=0, kc=None) == kv.OK  # empty batch: no-op
+    assert _append(g0, fn, n=1) == kv.ERR_INVALID_ARG
+
+
+def test_build_append_metadata_rejects_bad_arguments():
+    g = kv.Geom(2, 8, 128, 16, 64, 8, 0)
+    lib = kv.load()
+    assert lib.kvc8_build_append_metadata(ctypes.byref(g), None, None, None, None, FAKE, 1 << 20,
+                                          None, None) == kv.ERR_INVALID_ARG
+    assert lib.kvc8_build_append_metadata(ctypes.byref(g), None, FAKE, None, None, FAKE, 8,
+                                          None, None) == kv.ERR_WORKSPACE
