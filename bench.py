@@ -451,6 +451,65 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def result_line(args, world, w, nbytes, t, clocks, e2e, has_store):
+    """The JSON line of the GPU arm from the measured op times (t: ms per op)."""
+    peak, peak_kind = measured_peak()
+    total = nbytes["store"] + nbytes["gather"]
+    value = job_throughput(total, world, t["step_ms"])
+    fused = args.path == "fused"
+    timed_store = has_store and not fused and t["store_ms"] > 0
+    ops = {
+        "store": {"ms": round(t["store_ms"], 5),
+                  "GB_s": round(nbytes["store"] / (t["store_ms"] * 1e-3) / 1e9, 1) if timed_store else None,
+                  "tokens_per_s": round(w.num_tokens / (t["store_ms"] * 1e-3), 1) if timed_store else None,
+                  "bytes": nbytes["store"]},
+        "dequant_gather": {"ms": round(t["gather_ms"], 5),
+                           "kernels": "plan + fused append/gather" if fused else "plan + gather",
+                           "GB_s": round(nbytes["gather"] / (t["gather_ms"] * 1e-3) / 1e9, 1),
+                           "tokens_per_s": round(w.total_context / (t["gather_ms"] * 1e-3), 1),
+                           "bytes": nbytes["gather"]},
+    }
+    if fused:  # one op: the store is inside the fused launch
+        ops["store"] = {"ms": 0.0, "GB_s": None, "tokens_per_s": None, "bytes": 0,
+                        "note": "done inside the fused append + gather launch"}
+        ops["dequant_gather"]["appended_tokens_per_s"] = round(
+            w.num_tokens / (t["gather_ms"] * 1e-3), 1) if has_store else None
+    # the dominant kernel: the op with the larger device time
+    dom = "dequant_gather" if (t["gather_ms"] >= t["store_ms"] or not timed_store) else "store"
+    dom_bytes = nbytes["gather"] if dom == "dequant_gather" else nbytes["store"]
+    dom_ms = t["gather_ms"] if dom == "dequant_gather" else t["store_ms"]
+    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
+    kname = "gather" if dom == "dequant_gather" else "store"
+    if args.path == "bf16":
+        kname += "_bf16"
+    if fused:
+        kname = "append_gather"
+    traffic = ncu_traffic(args.workload).get(kname + "_kernel")
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t["step_ms"], 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if args.path == "bf16" else "f32",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD_TEXT[args.workload],
+                   "path": PATH_TEXT[args.path],
+                   "l2": "flushed before each timed op (256 MiB write, then 256 MiB read)",
+                   "hbm_frac_of_step": round(total / (t["step_ms"] * 1e-3) / 1e9 / peak, 4),
+                   "tokens_per_s": {"store": ops["store"]["tokens_per_s"],
+                                    "dequant_gather": ops["dequant_gather"]["tokens_per_s"]}},
+        "ops": ops,
+        "roofline": {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1),
+                     "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "peak_kind": peak_kind, "traffic": traffic,
+                     "algorithmic_bytes": dom_bytes},
+        "gpu_launches": args.steps * (3 if has_store and not fused else 2),
+        "clocks": clocks,
+        "e2e": e2e,
+        "wall_s": round(t["wall_s"], 3),
+    }
+    return line
+
+
 # ---------------------------------------------------------------------------- main
 
 def main():
@@ -478,59 +537,7 @@ def main():
         torch.distributed.init_process_group("nccl")
     w, nbytes, t, clocks, e2e, has_store = run_gpu(args, rank, world)
     if rank == 0:
-        peak, peak_kind = measured_peak()
-        total = nbytes["store"] + nbytes["gather"]
-        value = job_throughput(total, world, t["step_ms"])
-        fused = args.path == "fused"
-        ops = {
-            "store": {"ms": round(t["store_ms"], 5),
-                      "GB_s": round(nbytes["store"] / (t["store_ms"] * 1e-3) / 1e9, 1) if has_store else None,
-                      "tokens_per_s": round(w.num_tokens / (t["store_ms"] * 1e-3), 1) if has_store else None,
-                      "bytes": nbytes["store"]},
-            "dequant_gather": {"ms": round(t["gather_ms"], 5),
-                               "kernels": "plan + fused append/gather" if fused else "plan + gather",
-                               "GB_s": round(nbytes["gather"] / (t["gather_ms"] * 1e-3) / 1e9, 1),
-                               "tokens_per_s": round(w.total_context / (t["gather_ms"] * 1e-3), 1),
-                               "bytes": nbytes["gather"]},
-        }
-        if fused:  # one op: the store is inside the fused launch
-            ops["store"] = {"ms": 0.0, "GB_s": None, "tokens_per_s": None, "bytes": 0,
-                            "note": "done inside the fused append + gather launch"}
-            ops["dequant_gather"]["appended_tokens_per_s"] = round(
-                w.num_tokens / (t["gather_ms"] * 1e-3), 1) if has_store else None
-        # the dominant kernel: the op with the larger device time
-        dom = "dequant_gather" if (t["gather_ms"] >= t["store_ms"] or not has_store) else "store"
-        dom_bytes = nbytes["gather"] if dom == "dequant_gather" else nbytes["store"]
-        dom_ms = t["gather_ms"] if dom == "dequant_gather" else t["store_ms"]
-        achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
-        kname = "gather" if dom == "dequant_gather" else "store"
-        if args.path == "bf16":
-            kname += "_bf16"
-        if fused:
-            kname = "append_gather"
-        traffic = ncu_traffic(args.workload).get(kname + "_kernel")
-        line = {
-            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t["step_ms"], 5),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "bf16" if args.path == "bf16" else "f32",
-            "data": "synthetic",
-            "config": {"workload": WORKLOAD_TEXT[args.workload],
-                       "path": PATH_TEXT[args.path],
-                       "l2": "flushed before each timed op (256 MiB write, then 256 MiB read)",
-                       "hbm_frac_of_step": round(total / (t["step_ms"] * 1e-3) / 1e9 / peak, 4),
-                       "tokens_per_s": {"store": ops["store"]["tokens_per_s"],
-                                        "dequant_gather": ops["dequant_gather"]["tokens_per_s"]}},
-            "ops": ops,
-            "roofline": {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1),
-                         "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                         "peak_kind": peak_kind, "traffic": traffic,
-                         "algorithmic_bytes": dom_bytes},
-            "gpu_launches": args.steps * (3 if has_store and not fused else 2),
-            "clocks": clocks,
-            "e2e": e2e,
-            "wall_s": round(t["wall_s"], 3),
-        }
+        line = result_line(args, world, w, nbytes, t, clocks, e2e, has_store)
         if world == 1 and not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(w, args.path)
         print(json.dumps(line), flush=True)
