@@ -235,6 +235,10 @@ static kvc8_status append_args(const kvc8_geom *g, int64_t num_tokens, const voi
     if (num_tokens < 0) return KVC8_ERR_INVALID_ARG;
     if (num_tokens > INT32_MAX) return KVC8_ERR_UNSUPPORTED;  // token indices are 32-bit
     if (cu_q_lens == nullptr && num_tokens != g->num_seqs) return KVC8_ERR_INVALID_ARG;
+    // the fused kernel indexes its work items and appended rows in 32 bits
+    if ((int64_t)g->num_seqs * g->max_blocks_per_seq * g->kv_heads > (int64_t)INT32_MAX ||
+        num_tokens * 2 * g->kv_heads > (int64_t)INT32_MAX)
+        return KVC8_ERR_UNSUPPORTED;
     st = check_gather_args(g, key_cache, value_cache, key_scale, value_scale, block_table,
                            context_kv_lens, key_out, value_out, out_rows, out_tok_stride,
                            out_head_stride);

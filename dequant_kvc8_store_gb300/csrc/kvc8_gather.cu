@@ -209,12 +209,13 @@ __device__ __forceinline__ void store_chunk(uint16_t *p, const uint32_t *o) {
 }
 
 // Append part of the fused append + gather: row r = (token t, K|V, head h) of
-// the new tokens, one per warp.  Lane l holds values [8l, 8l + 8) of the row.
-// The codes follow the definition directly -- s = fl(amax / 127) (mode 0) or
-// the static scale, q = clamp(rne(fl(x / s)), -127, 127), 0 when s = 0 --
-// because an append is a handful of rows per sequence and its time is latency.
-// The output values are formed exactly as the gather forms them from the
-// cache: fl(float(q) * s), rounded to bf16 (RNE).
+// the new tokens, one per warp.  Lane l holds values [4l, 4l + 4) of each
+// 128-value chunk of the row (two chunks when D = 256).  The codes follow the
+// definition directly -- s = fl(amax / 127) (mode 0) or the static scale,
+// q = clamp(rne(fl(x / s)), -127, 127), 0 when s = 0 -- because an append is a
+// handful of rows per sequence and its time is latency.  The output values are
+// formed exactly as the gather forms them from the cache: fl(float(q) * s),
+// rounded to bf16 (RNE).
 template <int MODE, int CH>
 __device__ __forceinline__ void append_row(const GatherArgs &a, const AppendArgs &p, int64_t r,
                                            const int64_t *off, const float *s_tab) {
@@ -222,14 +223,21 @@ __device__ __forceinline__ void append_row(const GatherArgs &a, const AppendArgs
     const int B = a.g.num_seqs, MB = a.g.max_blocks_per_seq, NB = a.g.num_blocks;
     const int lane = threadIdx.x & 31;
     if (r >= p.num_tokens * 2 * H) return;  // warp-uniform
-    const int64_t t = r / (2 * H);
+    const int64_t t = (int64_t)((uint32_t)r / (uint32_t)(2 * H));  // r < 2^31
     const int u = (int)(r - t * 2 * H);
     const int kv = u >= H, h = u - kv * H;
-    const bool on = lane < (D >> 3);
-    uint4 x = make_uint4(0u, 0u, 0u, 0u);
-    if (on)
-        x = ld_stream_16((kv ? p.v_states : p.k_states) + t * p.x_tok_stride +
-                         (int64_t)h * p.x_head_stride + lane * 8);
+    const uint16_t *src = (kv ? p.v_states : p.k_states) + t * p.x_tok_stride +
+                          (int64_t)h * p.x_head_stride;
+    uint32_t x[2][2];
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+        const int d0 = c * 128 + lane * 4;
+        x[c][0] = x[c][1] = 0u;
+        if (d0 < D)
+            asm("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];"
+                : "=r"(x[c][0]), "=r"(x[c][1])
+                : "l"(src + d0));
+    }
 
     // slot of token t (warp-uniform)
     int b;
@@ -247,7 +255,8 @@ __device__ __forceinline__ void append_row(const GatherArgs &a, const AppendArgs
     }
     const int64_t ctx = ld_nc_s32(p.context_kv_lens + b);
     const int64_t pos = ctx + i_in_seq;
-    const int64_t lb = pos / bs;
+    // pos < 2^32: a 32-bit division (ctx and the token index are below 2^31)
+    const int64_t lb = pos >= 0 ? (int64_t)((uint32_t)pos / (uint32_t)bs) : -1;
     int32_t err = 0, blk = 0;
     if (bad_len || ctx < 0) {
         err = KVC8_DEV_BAD_LENGTH;
@@ -261,63 +270,60 @@ __device__ __forceinline__ void append_row(const GatherArgs &a, const AppendArgs
         if (lane == 0) report(a.dev_error, err);
         return;
     }
-    const int64_t slot = pos - lb * bs;
-
-    const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
-    float v[8];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        v[2 * k] = __uint_as_float(xw[k] << 16);
-        v[2 * k + 1] = __uint_as_float(xw[k] & 0xFFFF0000u);
-    }
-    float sc[8];
-    if (MODE == 0) {
-        float m = 0.0f;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(v[e]));
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-        const float s = __fdiv_rn(m, 127.0f);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) sc[e] = s;
-    } else {
-        constexpr int SPAD = CH + 4;
-        const int CPR = D / CH;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const int d = on ? lane * 8 + e : 0;
-            sc[e] = s_tab[((kv * H + h) * CPR + d / CH) * SPAD + d % CH];
-        }
-    }
-    int q[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e)
-        q[e] = sc[e] == 0.0f ? 0 : min(127, max(-127, __float2int_rn(__fdiv_rn(v[e], sc[e]))));
-
-    const int64_t row = ((int64_t)blk * H + h) * bs + slot;
-    if (on) {
-        const uint32_t c0 = __byte_perm(__byte_perm((uint32_t)q[0], (uint32_t)q[1], 0x0040),
-                                        __byte_perm((uint32_t)q[2], (uint32_t)q[3], 0x0040), 0x5410);
-        const uint32_t c1 = __byte_perm(__byte_perm((uint32_t)q[4], (uint32_t)q[5], 0x0040),
-                                        __byte_perm((uint32_t)q[6], (uint32_t)q[7], 0x0040), 0x5410);
-        st_8((kv ? p.v_cache : p.k_cache) + row * D + lane * 8, c0, c1);
-    }
-    if (MODE == 0 && lane == 0) (kv ? p.v_scale : p.k_scale)[row] = sc[0];
-
+    const int64_t row = ((int64_t)blk * H + h) * bs + (pos - lb * bs);
     const int64_t orow = off[b] + pos;
-    if (orow < 0 || orow >= a.out_rows) {
-        if (lane == 0) report(a.dev_error, KVC8_DEV_OUT_ROW_RANGE);
-        return;
-    }
-    if (on) {
-        uint32_t o[4];
+    const bool out_ok = orow >= 0 && orow < a.out_rows;
+    if (!out_ok && lane == 0) report(a.dev_error, KVC8_DEV_OUT_ROW_RANGE);
+
+    float s = 0.0f;  // mode 0: the row scale
+    if (MODE == 0) {
+        uint32_t m = 0u;  // |x| as bf16 bits: integer order = magnitude order
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-            o[k] = bf16x2_rn(__fmul_rn((float)q[2 * k], sc[2 * k]),
-                             __fmul_rn((float)q[2 * k + 1], sc[2 * k + 1]));
-        st_stream_16((kv ? a.v_out : a.k_out) + orow * a.out_tok_stride +
-                         (int64_t)h * a.out_head_stride + lane * 8,
-                     o[0], o[1], o[2], o[3]);
+        for (int c = 0; c < 2; ++c)
+            m = max(m, max(max(x[c][0] & 0x7FFFu, (x[c][0] >> 16) & 0x7FFFu),
+                           max(x[c][1] & 0x7FFFu, (x[c][1] >> 16) & 0x7FFFu)));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+        s = __fdiv_rn(__uint_as_float(m << 16), 127.0f);
+        if (lane == 0) (kv ? p.v_scale : p.k_scale)[row] = s;
+    }
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+        const int d0 = c * 128 + lane * 4;
+        if (d0 >= D) continue;
+        float sc[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            if (MODE == 0) {
+                sc[e] = s;
+            } else {
+                constexpr int SPAD = CH + 4;
+                const int d = d0 + e;
+                sc[e] = s_tab[((kv * H + h) * (D / CH) + d / CH) * SPAD + d % CH];
+            }
+        }
+        int q[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const uint32_t w = x[c][e >> 1];
+            const float v = __uint_as_float((e & 1) ? (w & 0xFFFF0000u) : (w << 16));
+            q[e] = sc[e] == 0.0f ? 0 : min(127, max(-127, __float2int_rn(__fdiv_rn(v, sc[e]))));
+        }
+        const uint32_t codes = __byte_perm(__byte_perm((uint32_t)q[0], (uint32_t)q[1], 0x0040),
+                                           __byte_perm((uint32_t)q[2], (uint32_t)q[3], 0x0040),
+                                           0x5410);
+        asm volatile("st.global.u32 [%0], %1;" ::"l"((kv ? p.v_cache : p.k_cache) + row * D + d0),
+                     "r"(codes)
+                     : "memory");
+        if (out_ok) {
+            const uint32_t o0 = bf16x2_rn(__fmul_rn((float)q[0], sc[0]), __fmul_rn((float)q[1], sc[1]));
+            const uint32_t o1 = bf16x2_rn(__fmul_rn((float)q[2], sc[2]), __fmul_rn((float)q[3], sc[3]));
+            asm volatile("st.global.cs.v2.u32 [%0], {%1, %2};" ::"l"(
+                             (kv ? a.v_out : a.k_out) + orow * a.out_tok_stride +
+                             (int64_t)h * a.out_head_stride + d0),
+                         "r"(o0), "r"(o1)
+                         : "memory");
+        }
     }
 }
 
@@ -327,7 +333,7 @@ __device__ __forceinline__ void append_row(const GatherArgs &a, const AppendArgs
 // APPEND: the fused append + gather; items [0, p.items) are append items
 // (kAppendRowsPerItem rows each), the gather items follow.
 template <int MODE, int CH, bool WIDE, bool APPEND>
-__global__ void __launch_bounds__(kGatherThreads)
+__global__ void __launch_bounds__(kGatherThreads, APPEND ? (MODE == 0 ? 6 : 4) : 0)
 gather_kernel(const GatherArgs a, const AppendArgs p) {
     constexpr int W = CH / 4;  // words per chunk
     constexpr int PER = 1;     // chunks per slab per thread per round
@@ -359,20 +365,28 @@ gather_kernel(const GatherArgs a, const AppendArgs p) {
     const int64_t items = hdr->total_tiles * H + (APPEND ? p.items : 0);
 
     int64_t item = blockIdx.x;
-    while (item < items) {
-        long long next = 0;
-        if (threadIdx.x == 0) next = (long long)atomicAdd(counter, 1ull) + gridDim.x;
-        if (APPEND && item < p.items) {
+    if (APPEND) {
+        // Items come in increasing order, so once a CTA draws a gather item it
+        // never draws an append item again: the append loop runs first.
+        while (item < p.items) {
+            long long next = 0;
+            if (threadIdx.x == 0) next = (long long)atomicAdd(counter, 1ull) + gridDim.x;
             append_row<MODE, CH>(a, p, item * kAppendRowsPerItem + (threadIdx.x >> 5), off, s_tab);
             if (threadIdx.x == 0) s_item = next;
             __syncthreads();
             item = s_item;
             __syncthreads();
-            continue;
         }
-        const int64_t gitem = APPEND ? item - p.items : item;
+    }
+    const int64_t first_gather = APPEND ? p.items : 0;
+    while (item < items) {
+        long long next = 0;
+        if (threadIdx.x == 0) next = (long long)atomicAdd(counter, 1ull) + gridDim.x;
+        const int64_t gitem = item - first_gather;
 
-        const int64_t tile = gitem / H;
+        // 32-bit division in append mode (the host keeps its item counts below
+        // 2^31); a 64-bit division there raised the kernel's register count
+        const int64_t tile = APPEND ? (int64_t)((uint32_t)gitem / (uint32_t)H) : gitem / H;
         const int r2 = (int)(gitem - tile * H);
         const int b = seq_of_tile(ts, B, tile);
         const int64_t j = tile - ts[b];

@@ -200,6 +200,8 @@ def test_append_gather_rejects_bad_arguments(fn):
     assert _append(g, fn, n=3, cu=None) == kv.ERR_INVALID_ARG  # decode form: one per sequence
     assert _append(g, fn, n=-1) == kv.ERR_INVALID_ARG
     assert _append(g, fn, n=1 << 31) == kv.ERR_UNSUPPORTED
+    assert _append(g, fn, n=1 << 27) == kv.ERR_UNSUPPORTED  # 2^27 tokens x 16 rows
+    assert _append(kv.Geom(1 << 20, 8, 128, 16, 64, 1 << 8, 0), fn) == kv.ERR_UNSUPPORTED
     assert _append(g, fn, ws=None) == kv.ERR_WORKSPACE
     assert _append(g, fn, wsb=16) == kv.ERR_WORKSPACE
     assert _append(kv.Geom(2, 8, 128, 16, 64, 8, 3), fn) == kv.ERR_INVALID_ARG
