@@ -141,12 +141,15 @@ class Oracle:
     # ---- row / tensor level ----------------------------------------------
 
     def quantize_rows(self, quant_mode: int, x_bits, static_scale=None):
-        """x_bits uint16 [n][H][D] -> (codes int8 [n][H][D], scales fp32 [n][H] or None)."""
+        """x_bits uint16 [n][H][D] -> (codes int8 [n][H][D], scales fp32 [n][H] or None).
+
+        static_scale: [H][D] for quant_mode 1, one scale per row [n][H] for
+        quant_mode 2 (in the cache, the scale of the row's block)."""
         x = _c(x_bits, np.uint16)
         n, H, D = x.shape
         q = np.empty((n, H, D), np.int8)
         s = np.empty((n, H), np.float32) if quant_mode == 0 else None
-        ss = _c(static_scale, np.float32) if quant_mode == 1 else None
+        ss = _c(static_scale, np.float32) if quant_mode in (1, 2) else None
         _check(self.lib.orc_quantize_rows(quant_mode, n, H, D, _ptr(x), _ptr(ss),
                                           _ptr(q), _ptr(s)), "orc_quantize_rows")
         return q, s
@@ -156,8 +159,9 @@ class Oracle:
         """Store in place into the numpy caches (and quant_mode-0 scale caches).
 
         k_bits/v_bits uint16 [N][H][D]; caches int8 [NB][H][bs][D]; k_scale /
-        v_scale fp32 [NB][H][bs] (quant_mode 0, written) or [H][D] (quant_mode
-        1, read); block_table int32 [B][MB]; cu_q_lens int32 [B+1] or None;
+        v_scale fp32 [NB][H][bs] (quant_mode 0, written), [H][D] (quant_mode
+        1, read) or [NB][H] (quant_mode 2, read); block_table int32 [B][MB];
+        cu_q_lens int32 [B+1] or None;
         context_kv_lens int32 [B].  Outputs must be C-contiguous.
         """
         for a in (k_cache, v_cache, k_scale, v_scale):

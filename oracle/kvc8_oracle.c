@@ -27,6 +27,7 @@
  *   store   x_d   = float(bf16 input)                         (exact widening)
  *           s     = max_d |x_d| / 127          (quant_mode 0, dynamic, per row)
  *           s_d   = static_scale[h][d]         (quant_mode 1, static, per channel)
+ *           s     = block_scale[blk][h]        (quant_mode 2, static, per block)
  *           q_d   = clamp(round_half_even(x_d / s), -127, 127), q_d = 0 if s == 0
  *           pos   = context_kv_lens[b] + i     (i-th new token of sequence b)
  *           cache[block_table[b][pos / bs]][h][pos % bs][d] = q_d
@@ -139,12 +140,14 @@ static int orc_slot(const int32_t *block_table, int max_blocks_per_seq,
 
 /* Quantise n rows of one kv-head set.  x: [n][H][D] bf16 bits, dense.
  * quant_mode 0: s_out[n][H] receives the per-row scale.
- * quant_mode 1: static_scale is [H][D]; s_out is not written. */
+ * quant_mode 1: static_scale is [H][D]; s_out is not written.
+ * quant_mode 2: static_scale is [n][H], the scale of each row (in the cache,
+ *               the scale of the row's block); s_out is not written. */
 int orc_quantize_rows(int quant_mode, int64_t n, int kv_heads, int head_dim,
                       const uint16_t *x, const float *static_scale,
                       int8_t *q_out, float *s_out)
 {
-    if (quant_mode != 0 && quant_mode != 1)
+    if (quant_mode < 0 || quant_mode > 2)
         return ORC_ERR_ARG;
     for (int64_t t = 0; t < n; ++t) {
         for (int h = 0; h < kv_heads; ++h) {
@@ -155,10 +158,14 @@ int orc_quantize_rows(int quant_mode, int64_t n, int kv_heads, int head_dim,
                 s_out[t * kv_heads + h] = s;
                 for (int d = 0; d < head_dim; ++d)
                     qrow[d] = orc_quantize_one(orc_bf16_to_f32(row[d]), s);
-            } else {
+            } else if (quant_mode == 1) {
                 for (int d = 0; d < head_dim; ++d)
                     qrow[d] = orc_quantize_one(orc_bf16_to_f32(row[d]),
                                                static_scale[h * head_dim + d]);
+            } else {
+                float s = static_scale[t * kv_heads + h];
+                for (int d = 0; d < head_dim; ++d)
+                    qrow[d] = orc_quantize_one(orc_bf16_to_f32(row[d]), s);
             }
         }
     }
@@ -170,6 +177,12 @@ int orc_quantize_rows(int quant_mode, int64_t n, int kv_heads, int head_dim,
  *   k_cache, v_cache   : int8 [num_blocks][H][block_size][D]
  *   k_scale, v_scale   : quant_mode 0 -> fp32 [num_blocks][H][block_size], written
  *                        quant_mode 1 -> fp32 [H][D], read
+ *                        quant_mode 2 -> fp32 [num_blocks][H], read
+ *                        (READING: [PR379] pass 1, "Must fix", and its
+ *                        "[CHECK]" note name per-block scales for
+ *                        quant_mode != 0 without a formula; here one static
+ *                        scale per physical block and kv head, owned by the
+ *                        caller like the per-channel table)
  *   block_table        : int32 [num_seqs][max_blocks_per_seq]
  *   cu_q_lens          : int32 [num_seqs + 1] prefix of new-token counts, or
  *                        NULL for pure decode (READING: one new token per
@@ -187,7 +200,7 @@ int orc_store(int quant_mode, int num_seqs, int64_t num_tokens, int kv_heads,
               float *k_scale, float *v_scale, const int32_t *block_table,
               const int32_t *cu_q_lens, const int32_t *context_kv_lens)
 {
-    if (quant_mode != 0 && quant_mode != 1)
+    if (quant_mode < 0 || quant_mode > 2)
         return ORC_ERR_ARG;
     const int64_t row_elems = (int64_t)kv_heads * head_dim;
     for (int b = 0; b < num_seqs; ++b) {
@@ -216,10 +229,14 @@ int orc_store(int quant_mode, int num_seqs, int64_t num_tokens, int kv_heads,
                         scale[dst_row] = s;
                         for (int d = 0; d < head_dim; ++d)
                             dst[d] = orc_quantize_one(orc_bf16_to_f32(row[d]), s);
-                    } else {
+                    } else if (quant_mode == 1) {
                         for (int d = 0; d < head_dim; ++d)
                             dst[d] = orc_quantize_one(orc_bf16_to_f32(row[d]),
                                                       scale[h * head_dim + d]);
+                    } else {
+                        float s = scale[(int64_t)blk * kv_heads + h];
+                        for (int d = 0; d < head_dim; ++d)
+                            dst[d] = orc_quantize_one(orc_bf16_to_f32(row[d]), s);
                     }
                 }
             }
@@ -258,7 +275,7 @@ int orc_dequant_gather(int quant_mode, int num_seqs, int kv_heads,
                        uint16_t *v_out, int64_t out_rows, int64_t tok_stride,
                        int64_t head_stride)
 {
-    if (quant_mode != 0 && quant_mode != 1)
+    if (quant_mode < 0 || quant_mode > 2)
         return ORC_ERR_ARG;
     int64_t acc = 0;
     for (int b = 0; b < num_seqs; ++b) {
@@ -281,8 +298,9 @@ int orc_dequant_gather(int quant_mode, int num_seqs, int kv_heads,
                     const int8_t *src = cache + src_row * head_dim;
                     uint16_t *dst = out + (off + p) * tok_stride + (int64_t)h * head_stride;
                     for (int d = 0; d < head_dim; ++d) {
-                        float s = quant_mode == 0 ? scale[src_row]
-                                                  : scale[h * head_dim + d];
+                        float s = quant_mode == 0   ? scale[src_row]
+                                  : quant_mode == 1 ? scale[h * head_dim + d]
+                                                    : scale[(int64_t)blk * kv_heads + h];
                         dst[d] = orc_dequantize_one(src[d], s);
                     }
                 }
@@ -304,7 +322,7 @@ int orc_dequant_positions(int quant_mode, int kv_heads, int head_dim,
                           const int32_t *sample_seq, const int64_t *sample_pos,
                           uint16_t *k_rows, uint16_t *v_rows)
 {
-    if (quant_mode != 0 && quant_mode != 1)
+    if (quant_mode < 0 || quant_mode > 2)
         return ORC_ERR_ARG;
     for (int64_t i = 0; i < n; ++i) {
         int32_t blk, slot;
@@ -319,7 +337,9 @@ int orc_dequant_positions(int quant_mode, int kv_heads, int head_dim,
             for (int h = 0; h < kv_heads; ++h) {
                 int64_t src_row = ((int64_t)blk * kv_heads + h) * block_size + slot;
                 for (int d = 0; d < head_dim; ++d) {
-                    float s = quant_mode == 0 ? scale[src_row] : scale[h * head_dim + d];
+                    float s = quant_mode == 0   ? scale[src_row]
+                              : quant_mode == 1 ? scale[h * head_dim + d]
+                                                : scale[(int64_t)blk * kv_heads + h];
                     rows[(i * kv_heads + h) * head_dim + d] =
                         orc_dequantize_one(cache[src_row * head_dim + d], s);
                 }

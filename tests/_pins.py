@@ -155,6 +155,16 @@ def pin_exact_quantize_random(orc):
             for d in range(D):
                 want = ex.expected_code(F(float(xf[t, h, d])), F(float(static[h, d])))
                 assert int(q1[t, h, d]) == want, (t, h, d)
+    # mode 2, one scale per row (the row's block scale), zero included
+    per_row = np.exp(rng.uniform(np.log(0.003), np.log(2.0), size=(x.shape[0], H))).astype(np.float32)
+    per_row[3, 1] = 0.0
+    q2, s2 = orc.quantize_rows(2, x, per_row)
+    assert s2 is None
+    for t in range(x.shape[0]):
+        for h in range(H):
+            for d in range(D):
+                want = ex.expected_code(F(float(xf[t, h, d])), F(float(per_row[t, h])))
+                assert int(q2[t, h, d]) == want, (t, h, d)
 
 
 def pin_exact_dequant_random(orc):
@@ -265,9 +275,12 @@ def _bruteforce_once(orc, rng, quant_mode, decode_null_cu):
     if quant_mode == 0:
         ks = rng.uniform(0.01, 0.1, size=(NB, H, bs)).astype(np.float32)
         vs = rng.uniform(0.01, 0.1, size=(NB, H, bs)).astype(np.float32)
-    else:
+    elif quant_mode == 1:
         ks = rng.uniform(0.005, 0.05, size=(H, D)).astype(np.float32)
         vs = rng.uniform(0.005, 0.05, size=(H, D)).astype(np.float32)
+    else:  # one scale per physical block and head, all distinct
+        ks = rng.uniform(0.005, 0.05, size=(NB, H)).astype(np.float32)
+        vs = rng.uniform(0.005, 0.05, size=(NB, H)).astype(np.float32)
     kc0, vc0, ks0, vs0 = kc.copy(), vc.copy(), ks.copy(), vs.copy()
     cu = None if decode_null_cu else np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
     orc.store(quant_mode, x, y, kc, vc, ks, vs, bt, cu, ctx_before.astype(np.int32))
@@ -282,8 +295,15 @@ def _bruteforce_once(orc, rng, quant_mode, decode_null_cu):
     phys = {}
     for (b, p), t in model.items():
         phys[(int(bt[b][p // bs]), p % bs)] = t
-    qx, sx = orc.quantize_rows(quant_mode, x, ks0 if quant_mode == 1 else None)
-    qy, sy = orc.quantize_rows(quant_mode, y, vs0 if quant_mode == 1 else None)
+    if quant_mode == 2:  # each token takes the scale of the physical block it lands in
+        tok_blk = np.zeros(N, np.int64)
+        for (b, p), t in model.items():
+            tok_blk[t] = bt[b][p // bs]
+        qx, sx = orc.quantize_rows(2, x, ks0[tok_blk])
+        qy, sy = orc.quantize_rows(2, y, vs0[tok_blk])
+    else:
+        qx, sx = orc.quantize_rows(quant_mode, x, ks0 if quant_mode == 1 else None)
+        qy, sy = orc.quantize_rows(quant_mode, y, vs0 if quant_mode == 1 else None)
     for blk in range(NB):
         for slot in range(bs):
             t = phys.get((blk, slot))
@@ -294,7 +314,7 @@ def _bruteforce_once(orc, rng, quant_mode, decode_null_cu):
                 for sc, s0, ss in ((ks, ks0, sx), (vs, vs0, sy)):
                     want = s0[blk, :, slot] if t is None else ss[t]
                     assert np.array_equal(sc[blk, :, slot], want), (blk, slot, t)
-    if quant_mode == 1:
+    if quant_mode != 0:  # static scales are read, never written
         assert np.array_equal(ks, ks0) and np.array_equal(vs, vs0)
 
     # gather: each output row is the dequantised physical row of its position
@@ -317,7 +337,8 @@ def _bruteforce_once(orc, rng, quant_mode, decode_null_cu):
                 for out, cache, sc in ((ko, kc, ks), (vo, vc, vs)):
                     for h in range(H):
                         for d in range(0, D, 5):
-                            s = sc[blk, h, slot] if quant_mode == 0 else sc[h, d]
+                            s = (sc[blk, h, slot] if quant_mode == 0 else
+                                 sc[h, d] if quant_mode == 1 else sc[blk, h])
                             want = ex.expected_dequant_bits(int(cache[blk, h, slot, d]),
                                                             F(float(s)))
                             assert int(out[row, h, d]) == want, (b, p, h, d)
@@ -328,6 +349,34 @@ def pin_placement_bruteforce(orc):
     rng = np.random.default_rng(2024)
     for it in range(24):
         _bruteforce_once(orc, rng, quant_mode=it % 2, decode_null_cu=(it % 6 == 5))
+    rng = np.random.default_rng(2025)
+    for it in range(12):  # per-block scales
+        _bruteforce_once(orc, rng, quant_mode=2, decode_null_cu=(it % 4 == 3))
+
+
+def pin_per_block_reduces_to_per_channel(orc):
+    """One scale for every block and head, c, is the per-channel table filled
+    with c: both modes must store and gather the same bits."""
+    rng = np.random.default_rng(31)
+    B, H, D, bs, MB = 3, 2, 16, 4, 3
+    NB = B * MB + 1
+    bt = rng.permutation(NB).astype(np.int32)[:B * MB].reshape(B, MB).copy()
+    q_lens = np.array([5, 1, 7])
+    ctx = np.array([2, 0, 4], np.int32)
+    cu = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
+    x = _random_bf16_rows(rng, int(q_lens.sum()), H, D)
+    y = _random_bf16_rows(rng, int(q_lens.sum()), H, D)
+    c = np.float32(0.0173)
+    pools = []
+    for mode, ks in ((1, np.full((H, D), c, np.float32)), (2, np.full((NB, H), c, np.float32))):
+        kc = np.zeros((NB, H, bs, D), np.int8)
+        vc = np.zeros((NB, H, bs, D), np.int8)
+        orc.store(mode, x, y, kc, vc, ks, ks.copy(), bt, cu, ctx)
+        lens = ctx + q_lens.astype(np.int32)
+        ko, vo = orc.dequant_gather(mode, kc, vc, ks, ks, bt, lens)
+        pools.append((kc, vc, ko, vo))
+    for a, b in zip(*pools):
+        assert np.array_equal(a, b)
 
 
 def pin_bounds_errors(orc):
@@ -427,4 +476,4 @@ def pin_bf16_bruteforce(orc):
 PINS = [pin_quantize_goldens, pin_dequant_goldens, pin_placement_golden,
         pin_exact_quantize_random, pin_exact_dequant_random, pin_invariants,
         pin_identity_table, pin_cumsum, pin_placement_bruteforce, pin_bounds_errors,
-        pin_bf16_placement_golden, pin_bf16_bruteforce]
+        pin_bf16_placement_golden, pin_bf16_bruteforce, pin_per_block_reduces_to_per_channel]

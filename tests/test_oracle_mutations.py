@@ -42,6 +42,12 @@ MUTATIONS = [
                                    "num_blocks, b, (int64_t)i,")]),
     ("bf16_gather_heads_swapped", [("uint16_t *dst = out + (off + p) * tok_stride + (int64_t)h * head_stride;\n                    for (int d = 0; d < head_dim; ++d)\n                        dst[d] = src[d];",
                                     "uint16_t *dst = out + (off + p) * tok_stride + (int64_t)(kv_heads - 1 - h) * head_stride;\n                    for (int d = 0; d < head_dim; ++d)\n                        dst[d] = src[d];")]),
+    ("block_scale_transposed", [("scale[(int64_t)blk * kv_heads + h]",
+                                 "scale[(int64_t)h * num_blocks + blk]")]),
+    ("block_scale_of_logical_block", [("float s = scale[(int64_t)blk * kv_heads + h];",
+                                       "float s = scale[(int64_t)(pos / block_size) * kv_heads + h];")]),
+    ("per_row_scale_of_head_zero", [("float s = static_scale[t * kv_heads + h];",
+                                     "float s = static_scale[t * kv_heads];")]),
 ]
 
 
