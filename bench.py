@@ -66,6 +66,8 @@ WORKLOAD_TEXT = {
              "U[0,16384], 8 x 128, block 64, 20480-block pool, static scales U[0.005,0.05]",
     "longctx": "long-context gather: 8 x 131072 cached tokens, 8 x 128, block 128, 8192 "
                "blocks, dynamic scales U[0.01,0.1]",
+    "prefill_block": "prefill store+gather with per-block scales: the prefill batch shapes, "
+                     "one static scale per (block, kv head) U[0.01,0.1]",
 }
 
 

@@ -32,7 +32,7 @@ kvc8_status check_geom(const kvc8_geom *g) {
     if (g->num_seqs < 0 || g->kv_heads < 1 || g->block_size < 1 || g->num_blocks < 1 ||
         g->max_blocks_per_seq < 1 || g->head_dim < 16)
         return KVC8_ERR_INVALID_ARG;
-    if (g->quant_mode != 0 && g->quant_mode != 1) return KVC8_ERR_INVALID_ARG;
+    if (g->quant_mode < 0 || g->quant_mode > 2) return KVC8_ERR_INVALID_ARG;
     if (g->head_dim % 16 != 0) return KVC8_ERR_INVALID_ARG;
     if (g->head_dim > kMaxHeadDim) return KVC8_ERR_UNSUPPORTED;
     // tile and unit counters are 32/64-bit; keep B * MB * 2H well inside int64

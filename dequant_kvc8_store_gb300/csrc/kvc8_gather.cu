@@ -164,8 +164,9 @@ __device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
     return r;
 }
 
-// One chunk of CH codes (CH/4 words) -> CH/2 packed bf16 pairs.  Mode 0: one
-// scale for the chunk; mode 1: per-channel scales sc[0..CH).
+// One chunk of CH codes (CH/4 words) -> CH/2 packed bf16 pairs.  Modes 0 and
+// 2: one scale for the chunk (the row's, or the block's); mode 1: per-channel
+// scales sc[0..CH).
 template <int CH, int MODE>
 __device__ __forceinline__ void dequant_chunk(const uint32_t *w, float s, const float *sc,
                                               uint32_t *o) {
@@ -175,7 +176,7 @@ __device__ __forceinline__ void dequant_chunk(const uint32_t *w, float s, const 
         codes_to_f32(w[j], f);
         float p[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) p[e] = __fmul_rn(f[e], MODE == 0 ? s : sc[4 * j + e]);
+        for (int e = 0; e < 4; ++e) p[e] = __fmul_rn(f[e], MODE != 1 ? s : sc[4 * j + e]);
         o[2 * j] = bf16x2_rn(p[0], p[1]);
         o[2 * j + 1] = bf16x2_rn(p[2], p[3]);
     }
@@ -211,7 +212,8 @@ __device__ __forceinline__ void store_chunk(uint16_t *p, const uint32_t *o) {
 // Append part of the fused append + gather: row r = (token t, K|V, head h) of
 // the new tokens, one per warp.  Lane l holds values [4l, 4l + 4) of each
 // 128-value chunk of the row (two chunks when D = 256).  The codes follow the
-// definition directly -- s = fl(amax / 127) (mode 0) or the static scale,
+// definition directly -- s = fl(amax / 127) (mode 0) or the static scale
+// (per channel, mode 1; per block, mode 2),
 // q = clamp(rne(fl(x / s)), -127, 127), 0 when s = 0 -- because an append is a
 // handful of rows per sequence and its time is latency.  The output values are
 // formed exactly as the gather forms them from the cache: fl(float(q) * s),
@@ -275,7 +277,8 @@ __device__ __forceinline__ void append_row(const GatherArgs &a, const AppendArgs
     const bool out_ok = orow >= 0 && orow < a.out_rows;
     if (!out_ok && lane == 0) report(a.dev_error, KVC8_DEV_OUT_ROW_RANGE);
 
-    float s = 0.0f;  // mode 0: the row scale
+    float s = 0.0f;  // modes 0 and 2: the row scale
+    if (MODE == 2) s = ld_nc_f32((kv ? p.v_scale : p.k_scale) + (int64_t)blk * H + h);
     if (MODE == 0) {
         uint32_t m = 0u;  // |x| as bf16 bits: integer order = magnitude order
 #pragma unroll
@@ -294,7 +297,7 @@ __device__ __forceinline__ void append_row(const GatherArgs &a, const AppendArgs
         float sc[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            if (MODE == 0) {
+            if (MODE != 1) {
                 sc[e] = s;
             } else {
                 constexpr int SPAD = CH + 4;
@@ -333,7 +336,7 @@ __device__ __forceinline__ void append_row(const GatherArgs &a, const AppendArgs
 // APPEND: the fused append + gather; items [0, p.items) are append items
 // (kAppendRowsPerItem rows each), the gather items follow.
 template <int MODE, int CH, bool WIDE, bool APPEND>
-__global__ void __launch_bounds__(kGatherThreads, APPEND ? (MODE == 0 ? 6 : 4) : 0)
+__global__ void __launch_bounds__(kGatherThreads, APPEND ? (MODE == 1 ? 4 : 6) : 0)
 gather_kernel(const GatherArgs a, const AppendArgs p) {
     constexpr int W = CH / 4;  // words per chunk
     constexpr int PER = 1;     // chunks per slab per thread per round
@@ -407,6 +410,7 @@ gather_kernel(const GatherArgs a, const AppendArgs p) {
             const float *rsc[2];
             const float *csc[2];
             uint16_t *dst[2];
+            float sblk[2];  // mode 2: the slab's block scale
 #pragma unroll
             for (int sl = 0; sl < 2; ++sl) {
                 const int u = 2 * r2 + sl;
@@ -414,6 +418,8 @@ gather_kernel(const GatherArgs a, const AppendArgs p) {
                 const int h = u - kv * H;
                 src[sl] = (kv ? a.v_cache : a.k_cache) + ((int64_t)blk * H + h) * bs * D;
                 rsc[sl] = (kv ? a.v_scale : a.k_scale) + ((int64_t)blk * H + h) * bs;
+                sblk[sl] = MODE == 2 ? ld_nc_f32((kv ? a.v_scale : a.k_scale) + (int64_t)blk * H + h)
+                                     : 0.0f;
                 csc[sl] = s_tab + (kv * H + h) * CPR * SPAD;
                 dst[sl] = (kv ? a.v_out : a.k_out) + row0 * a.out_tok_stride +
                           (int64_t)h * a.out_head_stride;
@@ -433,6 +439,7 @@ gather_kernel(const GatherArgs a, const AppendArgs p) {
                         if (c < nch) {
                             load_chunk<CH>(src[sl] + (int64_t)c * CH, w[sl][k]);
                             if (MODE == 0) s[sl][k] = ld_nc_f32(rsc[sl] + c / CPR);
+                            if (MODE == 2) s[sl][k] = sblk[sl];
                         }
                     }
                 }
@@ -520,8 +527,11 @@ cudaError_t launch_gather_any(const GatherArgs &a, const AppendArgs &p, bool use
     if (a.g.quant_mode == 0)
         return wide ? launch_gather_mode<0, true, APPEND>(a, p, use_pdl, stream)
                     : launch_gather_mode<0, false, APPEND>(a, p, use_pdl, stream);
-    return wide ? launch_gather_mode<1, true, APPEND>(a, p, use_pdl, stream)
-                : launch_gather_mode<1, false, APPEND>(a, p, use_pdl, stream);
+    if (a.g.quant_mode == 1)
+        return wide ? launch_gather_mode<1, true, APPEND>(a, p, use_pdl, stream)
+                    : launch_gather_mode<1, false, APPEND>(a, p, use_pdl, stream);
+    return wide ? launch_gather_mode<2, true, APPEND>(a, p, use_pdl, stream)
+                : launch_gather_mode<2, false, APPEND>(a, p, use_pdl, stream);
 }
 
 }  // namespace

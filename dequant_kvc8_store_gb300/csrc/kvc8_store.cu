@@ -27,7 +27,9 @@
 // within about 2^-21 relative of a half-integer; rare), the group of four
 // values is recomputed with __fdiv_rn + __float2int_rn.
 //
-// Static mode (s per channel; y = fl(x * fl(1/s)) clamped to [-127, 127]):
+// Static modes (s per channel, quant_mode 1, from a shared-memory table; or s
+// per block and kv head, quant_mode 2, read once per row; y = fl(x * fl(1/s))
+// clamped to [-127, 127]):
 // the relative error of y against t = x/s is at most 2^-23 + 2^-48, so
 // |y - t| < 1.55e-5 for |t| <= 130 and fl(t) is within half an ulp of t
 // (<= 7.7e-6 below 256).  If y lies more than 2^-15 from every half-integer,
@@ -111,7 +113,8 @@ __device__ __forceinline__ void store_codes16(int8_t *p, const uint32_t c[4]) {
                  : "memory");
 }
 
-// E values per lane (16 or 32), LANES lanes per row, MODE 0 dynamic / 1 static,
+// E values per lane (16 or 32), LANES lanes per row, MODE 0 dynamic / 1 static
+// per channel / 2 static per block,
 // V32: 32-byte aligned rows (256-bit loads and stores).
 template <int E, int LANES, int MODE, bool V32>
 __global__ void __launch_bounds__(kWarpsPerCta * 32, 3)
@@ -147,7 +150,7 @@ store_kernel(const StoreArgs a) {
             r_tab[m] = __frcp_rn(sm);
         }
         __syncthreads();
-    } else {
+    } else if (MODE == 1) {
         int ok = 1;
         for (int i = threadIdx.x; i < 2 * H * D; i += blockDim.x) {
             const float sc = i < H * D ? ld_nc_f32(a.k_scale + i) : ld_nc_f32(a.v_scale + (i - H * D));
@@ -253,6 +256,17 @@ store_kernel(const StoreArgs a) {
                         s_rows[k] = __fdiv_rn(__uint_as_float(mag << 16), 127.0f);
                         r_rows[k] = 0.0f;  // exact path for the whole row
                     }
+                } else if (MODE == 2 && p0 + k < passes) {
+                    // the row's block scale; a zero reciprocal sends the row
+                    // to the exact path
+                    const int row = (p0 + k) * RPP + sub;
+                    if (row < rows) {
+                        const int kv = row >= H;
+                        const int h = row - kv * H;
+                        const float sb = ld_nc_f32((kv ? a.v_scale : a.k_scale) + (int64_t)blk * H + h);
+                        s_rows[k] = sb;
+                        r_rows[k] = recip_ok(sb) ? __frcp_rn(sb) : 0.0f;
+                    }
                 }
             }
 
@@ -269,7 +283,7 @@ store_kernel(const StoreArgs a) {
                 const float *st = (kv ? a.v_scale : a.k_scale) + (int64_t)h * D + c * E;  // static mode
 
                 uint32_t cw[W / 2];  // packed codes, four per word
-                const bool force_exact = (MODE == 0) ? (r_row == 0.0f) : !all_fast;
+                const bool force_exact = (MODE == 1) ? !all_fast : (r_row == 0.0f);
                 // Dynamic mode: r_lo <= r (1 - 2^-23) and r_hi >= r (1 + 2^-23)
                 // bracket every value fl(x / s) can take, so when x r_lo and
                 // x r_hi round to the same integer, so does fl(x / s).
@@ -293,8 +307,9 @@ store_kernel(const StoreArgs a) {
                             differ |= (__float_as_uint(m2.x) ^ __float_as_uint(h2.x)) |
                                       (__float_as_uint(m2.y) ^ __float_as_uint(h2.y));
                         } else {
-                            const float2 r2 = on ? *reinterpret_cast<const float2 *>(rt + 2 * (i + e))
-                                                 : make_float2(1.0f, 1.0f);
+                            const float2 r2 = MODE == 2 ? make_float2(r_row, r_row)
+                                              : on ? *reinterpret_cast<const float2 *>(rt + 2 * (i + e))
+                                                   : make_float2(1.0f, 1.0f);
                             float2 y2 = __fmul2_rn(x2, r2);
                             y2.x = fminf(fmaxf(y2.x, -kSatClamp), kSatClamp);
                             y2.y = fminf(fmaxf(y2.y, -kSatClamp), kSatClamp);
@@ -315,7 +330,8 @@ store_kernel(const StoreArgs a) {
                             const uint32_t wi = w[k][i + (e >> 1)];
                             const float x = __uint_as_float((e & 1) ? (wi & 0xFFFF0000u) : (wi << 16));
                             const int j = 2 * i + e;
-                            q[e] = quant_one(x, MODE == 0 ? s_row : ld_nc_f32(st + j), MODE == 0 ? r_row : rt[j]);
+                            q[e] = MODE == 1 ? quant_one(x, ld_nc_f32(st + j), rt[j])
+                                             : quant_one(x, s_row, r_row);
                         }
                         word = pack_lo_bytes((uint32_t)q[0], (uint32_t)q[1], (uint32_t)q[2], (uint32_t)q[3]);
                     }
@@ -344,7 +360,8 @@ template <int E, int LANES, int MODE, bool V32>
 cudaError_t launch_variant(const StoreArgs &a, cudaStream_t stream) {
     auto kern = store_kernel<E, LANES, MODE, V32>;
     const int C = a.g.head_dim / E;
-    const size_t smem = MODE == 1 ? sizeof(float) * 2 * a.g.kv_heads * C * (E + 2) : sizeof(float) * 256;
+    const size_t smem = MODE == 1 ? sizeof(float) * 2 * a.g.kv_heads * C * (E + 2)
+                        : MODE == 0 ? sizeof(float) * 256 : 0;
     static OccCache cache;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -400,7 +417,9 @@ cudaError_t launch_store(const StoreArgs &a, cudaStream_t stream) {
                      a.x_head_stride % 16 == 0;
     if (a.g.quant_mode == 0)
         return v32 ? launch_mode<0, true>(a, stream) : launch_mode<0, false>(a, stream);
-    return v32 ? launch_mode<1, true>(a, stream) : launch_mode<1, false>(a, stream);
+    if (a.g.quant_mode == 1)
+        return v32 ? launch_mode<1, true>(a, stream) : launch_mode<1, false>(a, stream);
+    return v32 ? launch_mode<2, true>(a, stream) : launch_mode<2, false>(a, stream);
 }
 
 }  // namespace kvc8

@@ -170,6 +170,7 @@ def make_workload(name: str, *, q_lens, ctx_before, kv_heads: int, head_dim: int
                   max_blocks_per_seq: Optional[int] = None, decode_null_cu: bool = False,
                   outlier_channels: int = 0, outlier_gain: float = 20.0,
                   static_scale_range=(0.005, 0.05), pool_scale_range=(0.01, 0.1),
+                  block_scale_range=(0.01, 0.1),
                   gather_only: bool = False, with_store: bool = True) -> Workload:
     """General seeded workload.
 
@@ -205,8 +206,12 @@ def make_workload(name: str, *, q_lens, ctx_before, kv_heads: int, head_dim: int
         lo, hi = static_scale_range
         k_scale = random_uniform_f32(H * D, lo, hi, seed, _S_KS).reshape(H, D)
         v_scale = random_uniform_f32(H * D, lo, hi, seed, _S_VS).reshape(H, D)
+    elif quant_mode == 2:
+        lo, hi = block_scale_range
+        k_scale = random_uniform_f32(num_blocks * H, lo, hi, seed, _S_KS).reshape(num_blocks, H)
+        v_scale = random_uniform_f32(num_blocks * H, lo, hi, seed, _S_VS).reshape(num_blocks, H)
     else:
-        raise ValueError("quant_mode must be 0 or 1")
+        raise ValueError("quant_mode must be 0, 1 or 2")
     k_states = v_states = cu = None
     if not gather_only and with_store:
         N = int(q_lens.sum())
@@ -276,8 +281,17 @@ def longctx(seed: int = 1004) -> Workload:
                          quant_mode=0, seed=seed, gather_only=True)
 
 
+def prefill_block(seed: int = 1005) -> Workload:
+    """The prefill batch with one static scale per (block, kv head)."""
+    rng = np.random.default_rng([seed, 99])
+    q = rng.integers(512, 4096, size=16, endpoint=True)
+    return make_workload("prefill_block", q_lens=q, ctx_before=np.zeros(16, np.int64),
+                         kv_heads=8, head_dim=128, block_size=128, num_blocks=1024,
+                         max_blocks_per_seq=32, quant_mode=2, seed=seed, outlier_channels=4)
+
+
 NAMED = {"tiny": tiny, "prefill": prefill, "decode": decode, "mixed": mixed,
-         "longctx": longctx}
+         "longctx": longctx, "prefill_block": prefill_block}
 
 
 def algorithmic_bytes(w: Workload) -> dict:
@@ -296,7 +310,22 @@ def algorithmic_bytes(w: Workload) -> dict:
     per_row_scale = 4 if w.quant_mode == 0 else 0
     store = rows_store * (2 * D + D + per_row_scale) + (table if w.num_tokens else 0)
     gather = rows_gather * (D + per_row_scale + 2 * D) + (table if w.total_context else 0)
+    if w.quant_mode == 2:  # one 4-byte scale per (block, head) that the op touches
+        store += 4 * 2 * H * _blocks_touched(w, new_only=True)
+        gather += 4 * 2 * H * _blocks_touched(w, new_only=False)
     return {"store": int(store), "gather": int(gather)}
+
+
+def _blocks_touched(w: Workload, new_only: bool) -> int:
+    """Logical blocks that hold the new tokens (new_only) or any gathered
+    position, summed over sequences."""
+    bs = w.block_size
+    end = w.context_lengths.astype(np.int64)
+    start = w.context_kv_lens.astype(np.int64) if new_only else np.zeros_like(end)
+    has = end > start
+    first = start // bs
+    last = (end - 1) // bs
+    return int(np.where(has, last - first + 1, 0).sum())
 
 
 def algorithmic_bytes_bf16(w: Workload) -> dict:

@@ -83,11 +83,14 @@ enum {
 
 /* Geometry of one paged cache and one batch.  quant_mode: 0 = dynamic scale
  * per (token, kv head), kept in a scale cache beside the codes; 1 = static
- * scale per (kv head, channel), passed in.  [PR379] (every pass: the store is
- * a symmetric int8 quantisation against a passed-in per-channel scale; the
- * docstring says per_channal) describes the static form; the dynamic form
- * stores its per-row scales where the pass-1 "Must fix" expects per-block
- * scale shapes. */
+ * scale per (kv head, channel), passed in; 2 = static scale per (physical
+ * block, kv head), passed in.  [PR379] (every pass: the store is a symmetric
+ * int8 quantisation against a passed-in per-channel scale; the docstring says
+ * per_channal) describes the per-channel form; the dynamic form stores its
+ * per-row scales where the pass-1 "Must fix" expects per-block scale shapes,
+ * and mode 2 is the plain per-block reading of that same passage and of the
+ * pass-1 "[CHECK]" note (quant_mode != 0 is per-block), one caller-owned
+ * scale for every row of a block. */
 typedef struct kvc8_geom {
     int32_t num_seqs;           /* B >= 0 */
     int32_t kv_heads;           /* H >= 1 */
@@ -95,7 +98,7 @@ typedef struct kvc8_geom {
     int32_t block_size;         /* bs >= 1 */
     int32_t num_blocks;         /* NB >= 1 */
     int32_t max_blocks_per_seq; /* MB >= 1 */
-    int32_t quant_mode;         /* 0 or 1 */
+    int32_t quant_mode;         /* 0, 1 or 2 */
 } kvc8_geom;
 
 /* Human-readable name of a status code (static string). */
@@ -127,7 +130,8 @@ int32_t kvc8_version(void);
  *   value_cache    int8 [NB][H][bs][D], written in place
  *   key_scale,
  *   value_scale    mode 0: fp32 [NB][H][bs] scale caches, written in place;
- *                  mode 1: fp32 [H][D] static scales, read only
+ *                  mode 1: fp32 [H][D] static scales, read only;
+ *                  mode 2: fp32 [NB][H] block scales, read only
  *   block_table    int32 [B][MB]
  *   cu_q_lens      int32 [B+1], cu_q_lens[0] = 0, non-decreasing, last = N;
  *                  or NULL for pure decode: one new token per sequence, token
@@ -185,7 +189,8 @@ kvc8_status kvc8_build_metadata(const kvc8_geom *g, const int32_t *context_lengt
  *   out[(off_b + p) * out_tok_stride + h * out_head_stride + d]
  *       = bf16(fp32(cache[blk][h][slot][d]) * s)
  * with blk = block_table[b][p / bs], slot = p % bs, s = scale_cache[blk][h][slot]
- * (mode 0) or static_scale[h][d] (mode 1), and off_b as in
+ * (mode 0), static_scale[h][d] (mode 1) or block_scale[blk][h] (mode 2), and
+ * off_b as in
  * kvc8_build_metadata.  This is the pages' per-sequence loop (list-comprehension
  * concat of the sequence's blocks, dequant_from_cache, slice to the context,
  * transpose to [tokens, heads, dim], in-place write at the offset) as one
@@ -198,7 +203,8 @@ kvc8_status kvc8_build_metadata(const kvc8_geom *g, const int32_t *context_lengt
  * gather launch overlaps the plan's tail (programmatic dependent launch).
  *
  *   key_cache, value_cache   int8 [NB][H][bs][D]
- *   key_scale, value_scale   mode 0: fp32 [NB][H][bs]; mode 1: fp32 [H][D]
+ *   key_scale, value_scale   mode 0: fp32 [NB][H][bs]; mode 1: fp32 [H][D];
+ *                            mode 2: fp32 [NB][H]
  *   block_table              int32 [B][MB]
  *   context_lengths          int32 [B]
  *   context_seq_offset       int64 [B] or NULL (exclusive prefix sum)

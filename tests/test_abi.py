@@ -59,7 +59,7 @@ def test_store_rejects_bad_geometry():
               max_blocks_per_seq=8, quant_mode=0)
     for field, bad, want in [("head_dim", 24, kv.ERR_INVALID_ARG), ("head_dim", 8, kv.ERR_INVALID_ARG),
                              ("head_dim", 512, kv.ERR_UNSUPPORTED),
-                             ("quant_mode", 2, kv.ERR_INVALID_ARG),
+                             ("quant_mode", 3, kv.ERR_INVALID_ARG),
                              ("kv_heads", 0, kv.ERR_INVALID_ARG),
                              ("block_size", 0, kv.ERR_INVALID_ARG),
                              ("num_blocks", 0, kv.ERR_INVALID_ARG),

@@ -110,6 +110,15 @@ SMALL = [
          block_size=32, num_blocks=30, quant_mode=0),
     dict(q_lens=[41, 1, 70], ctx_before=[0, 9, 31], kv_heads=12, head_dim=256,
          block_size=16, num_blocks=40, quant_mode=1),
+    # one static scale per (block, kv head)
+    dict(q_lens=[0, 1, 17, 40, 3], ctx_before=[0, 5, 16, 30, 0], kv_heads=2, head_dim=64,
+         block_size=16, num_blocks=40, quant_mode=2),
+    dict(q_lens=[33, 7], ctx_before=[5, 60], kv_heads=3, head_dim=48, block_size=8,
+         num_blocks=40, quant_mode=2),
+    dict(q_lens=[1] * 7, ctx_before=[0, 1, 15, 16, 17, 100, 63], kv_heads=8, head_dim=128,
+         block_size=16, num_blocks=64, quant_mode=2, decode_null_cu=True),
+    dict(q_lens=[77, 3, 140], ctx_before=[5, 0, 60], kv_heads=16, head_dim=128,
+         block_size=32, num_blocks=30, quant_mode=2, block_scale_range=(0.002, 0.5)),
 ]
 
 
@@ -244,6 +253,39 @@ def test_static_scales_extremes():
     check_full(_set_states(w, gen(), gen()))
 
 
+def test_block_scales_extremes():
+    """Per-block scales: exact ties against each token's block scale (s = 2^e,
+    x = (j + 1/2) s), saturation, zero scales, and scales whose reciprocal leaves
+    the normal range."""
+    rng = np.random.default_rng(83)
+    w = W.make_workload("block", q_lens=[50, 14, 30], ctx_before=[0, 3, 17], kv_heads=2,
+                        head_dim=128, block_size=16, num_blocks=24, quant_mode=2, seed=83)
+    N, H, D = w.num_tokens, w.kv_heads, w.head_dim
+    NB = w.num_blocks
+    s = np.exp2(rng.integers(-10, 4, size=(NB, H))).astype(np.float32)
+    s[0::6, 0] = 0.0
+    s[1::6, 1] = np.float32(1e-38)   # below 2^-120: exact path
+    s[2::6, 0] = np.float32(3e38)    # above 2^120: exact path
+    s[3::6, 1] = np.float32(1e-30)   # reciprocal 1e30: saturates on the fast path
+    s[4::6, 0] = np.float32(0.0049)  # saturating for N(0,1) x 50
+    # the block each new token lands in
+    tok_blk = np.empty(N, np.int64)
+    t = 0
+    for b, q in enumerate(w.q_lens()):
+        for i in range(int(q)):
+            pos = int(w.context_kv_lens[b]) + i
+            tok_blk[t] = w.block_table[b][pos // w.block_size]
+            t += 1
+    def gen(scale):
+        j = rng.integers(-130, 130, size=(N, H, D)).astype(np.float64)
+        x = (j + 0.5) * scale[tok_blk][:, :, None].astype(np.float64)
+        x[:, :, 16:32] = rng.standard_normal((N, H, 16)) * 50
+        return _f32_to_bits(np.clip(x, -1e38, 1e38))  # finite inputs only
+    w.k_scale = s
+    w.v_scale = (s * np.float32(0.5)).astype(np.float32)
+    check_full(_set_states(w, gen(w.k_scale), gen(w.v_scale)))
+
+
 def test_subnormal_scales_in_gather():
     """Mode-0 scale caches with subnormal and zero scales (prefilled, not
     stored): fp32 products that are subnormal must round to bf16 like the
@@ -371,3 +413,13 @@ def test_full_mixed():
 
 def test_full_longctx():
     _check_full_size(W.longctx())
+
+
+def test_full_prefill_block():
+    w = W.prefill_block()
+    d = _check_full_size(w)
+    ko, vo = oracle.dequant_gather(2, w.k_cache, w.v_cache, w.k_scale, w.v_scale,
+                                   w.block_table, w.context_lengths)
+    gk, gv = d.host_outputs()
+    _assert_bits_equal(gk, ko, "k_out")
+    _assert_bits_equal(gv, vo, "v_out")
