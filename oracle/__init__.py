@@ -120,6 +120,9 @@ class Oracle:
         lib.orc_gather_bf16.argtypes = [i32, i32, i32, i32, i32, i32, P, P, P, P, P, P, P,
                                         i64, i64, i64]
         lib.orc_gather_bf16.restype = i32
+        lib.orc_paged_decode_attention.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32, P, P,
+                                                   P, P, P, P, P, ctypes.c_double, P]
+        lib.orc_paged_decode_attention.restype = i32
         self.lib = lib
         self.path = lib_path
 
@@ -271,6 +274,28 @@ class Oracle:
                                         H * D, D), "orc_gather_bf16")
         return k_out, v_out
 
+    def paged_decode_attention(self, quant_mode, query_bits, k_cache, v_cache, k_scale, v_scale,
+                               block_table, context_lengths, softmax_scale):
+        """Decode attention of query_bits (bf16 bits [B][Hq][D]) over the paged
+        int8 cache; returns the unrounded fp64 output [B][Hq][D]."""
+        qb = _c(query_bits, np.uint16)
+        kc, vc = _c(k_cache, np.int8), _c(v_cache, np.int8)
+        ks, vs = _c(k_scale, np.float32), _c(v_scale, np.float32)
+        bt = _c(block_table, np.int32)
+        ctx = _c(context_lengths, np.int32)
+        NB, H, bs, D = kc.shape
+        B, MB = bt.shape
+        hq = qb.shape[1]
+        if hq % H != 0 or qb.shape != (B, hq, D):
+            raise ValueError("query must be [B][G*H][D]")
+        out = np.empty((B, hq, D), np.float64)
+        _check(self.lib.orc_paged_decode_attention(quant_mode, B, H, hq // H, D, bs, NB, MB,
+                                                   _ptr(qb), _ptr(kc), _ptr(vc), _ptr(ks),
+                                                   _ptr(vs), _ptr(bt), _ptr(ctx),
+                                                   float(softmax_scale), _ptr(out)),
+               "orc_paged_decode_attention")
+        return out
+
     def slots(self, block_table, block_size, num_blocks, seq, pos):
         """Physical (block, slot) arrays for (seq, pos) pairs; -1 where out of range."""
         bt = _c(block_table, np.int32)
@@ -301,6 +326,7 @@ def __getattr__(name):
     # module-level shortcuts: oracle.store(...), oracle.dequant_gather(...), ...
     if name in {"quantize_value", "dequantize_value", "round_to_bf16", "row_scale",
                 "quantize_rows", "store", "exclusive_cumsum", "dequant_gather",
-                "dequant_positions", "slots", "store_bf16", "gather_bf16"}:
+                "dequant_positions", "slots", "store_bf16", "gather_bf16",
+                "paged_decode_attention"}:
         return getattr(default(), name)
     raise AttributeError(name)

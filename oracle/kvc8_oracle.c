@@ -460,3 +460,90 @@ int orc_gather_bf16(int num_seqs, int kv_heads, int head_dim, int block_size,
     }
     return ORC_OK;
 }
+
+/* ---- paged decode attention over the int8 cache ---------------------------
+ * MojoPagedDecodeGQA of the "Mojo Opset" README ("Op List", Attention): one
+ * decode query per sequence attends over the paged cache.  The pages give no
+ * formula; READING: the standard grouped-query scaled dot-product attention,
+ * over the values the dequant-gather produces, i.e. the bf16 rows
+ * bf16_rne(float(q) * s) of the cache, so that the fused op equals the
+ * dequant-gather followed by attention:
+ *   kv head of query head j     h = j / group       (group = Hq / H)
+ *   score_p = softmax_scale * sum_d query[b][j][d] * K'[b][p][h][d]
+ *   w_p     = exp(score_p - max_p score_p) / sum_p exp(score_p - max)
+ *   out[b][j][d] = sum_p w_p * V'[b][p][h][d]        (p < context_lengths[b])
+ * computed in fp64 and returned unrounded; an empty context gives 0.
+ *   query : bf16 bits [num_seqs][Hq][D], dense;  out : fp64 [num_seqs][Hq][D]. */
+int orc_paged_decode_attention(int quant_mode, int num_seqs, int kv_heads, int group,
+                               int head_dim, int block_size, int num_blocks,
+                               int max_blocks_per_seq, const uint16_t *query,
+                               const int8_t *k_cache, const int8_t *v_cache,
+                               const float *k_scale, const float *v_scale,
+                               const int32_t *block_table, const int32_t *context_lengths,
+                               double softmax_scale, double *out)
+{
+    if (quant_mode < 0 || quant_mode > 2 || group < 1)
+        return ORC_ERR_ARG;
+    const int hq = kv_heads * group;
+    for (int b = 0; b < num_seqs; ++b) {
+        int64_t len = context_lengths[b];
+        for (int j = 0; j < hq; ++j) {
+            int h = j / group;
+            const uint16_t *qv = query + ((int64_t)b * hq + j) * head_dim;
+            double *o = out + ((int64_t)b * hq + j) * head_dim;
+            for (int d = 0; d < head_dim; ++d)
+                o[d] = 0.0;
+            if (len <= 0)
+                continue;
+            /* pass 1: the largest score */
+            double mx = -HUGE_VAL;
+            for (int64_t p = 0; p < len; ++p) {
+                int32_t blk, slot;
+                int rc = orc_slot(block_table, max_blocks_per_seq, block_size,
+                                  num_blocks, b, p, &blk, &slot);
+                if (rc != ORC_OK)
+                    return rc;
+                int64_t row = ((int64_t)blk * kv_heads + h) * block_size + slot;
+                double dot = 0.0;
+                for (int d = 0; d < head_dim; ++d) {
+                    float s = quant_mode == 0   ? k_scale[row]
+                              : quant_mode == 1 ? k_scale[h * head_dim + d]
+                                                : k_scale[(int64_t)blk * kv_heads + h];
+                    double kd = orc_bf16_to_f32(orc_dequantize_one(k_cache[row * head_dim + d], s));
+                    dot += (double)orc_bf16_to_f32(qv[d]) * kd;
+                }
+                double sc = softmax_scale * dot;
+                if (sc > mx)
+                    mx = sc;
+            }
+            /* pass 2: weights and the weighted sum of V' rows */
+            double total = 0.0;
+            for (int64_t p = 0; p < len; ++p) {
+                int32_t blk, slot;
+                if (orc_slot(block_table, max_blocks_per_seq, block_size, num_blocks, b, p,
+                             &blk, &slot) != ORC_OK)
+                    return ORC_ERR_BOUNDS;
+                int64_t row = ((int64_t)blk * kv_heads + h) * block_size + slot;
+                double dot = 0.0;
+                for (int d = 0; d < head_dim; ++d) {
+                    float s = quant_mode == 0   ? k_scale[row]
+                              : quant_mode == 1 ? k_scale[h * head_dim + d]
+                                                : k_scale[(int64_t)blk * kv_heads + h];
+                    double kd = orc_bf16_to_f32(orc_dequantize_one(k_cache[row * head_dim + d], s));
+                    dot += (double)orc_bf16_to_f32(qv[d]) * kd;
+                }
+                double w = exp(softmax_scale * dot - mx);
+                total += w;
+                for (int d = 0; d < head_dim; ++d) {
+                    float s = quant_mode == 0   ? v_scale[row]
+                              : quant_mode == 1 ? v_scale[h * head_dim + d]
+                                                : v_scale[(int64_t)blk * kv_heads + h];
+                    o[d] += w * orc_bf16_to_f32(orc_dequantize_one(v_cache[row * head_dim + d], s));
+                }
+            }
+            for (int d = 0; d < head_dim; ++d)
+                o[d] /= total;
+        }
+    }
+    return ORC_OK;
+}

@@ -473,7 +473,85 @@ def pin_bf16_bruteforce(orc):
                 row += 1
 
 
+# ---- paged decode attention over the int8 cache ------------------------------
+
+def _attention_case(rng, B=3, H=2, G=2, D=16, bs=4, MB=5, mode=0, lens=None):
+    NB = B * MB + 2
+    kc = rng.integers(-127, 128, size=(NB, H, bs, D)).astype(np.int8)
+    vc = rng.integers(-127, 128, size=(NB, H, bs, D)).astype(np.int8)
+    if mode == 0:
+        ks = rng.uniform(0.01, 0.1, size=(NB, H, bs)).astype(np.float32)
+        vs = rng.uniform(0.01, 0.1, size=(NB, H, bs)).astype(np.float32)
+    elif mode == 1:
+        ks = rng.uniform(0.005, 0.05, size=(H, D)).astype(np.float32)
+        vs = rng.uniform(0.005, 0.05, size=(H, D)).astype(np.float32)
+    else:
+        ks = rng.uniform(0.005, 0.05, size=(NB, H)).astype(np.float32)
+        vs = rng.uniform(0.005, 0.05, size=(NB, H)).astype(np.float32)
+    bt = rng.permutation(NB).astype(np.int32)[:B * MB].reshape(B, MB).copy()
+    if lens is None:
+        lens = rng.integers(0, MB * bs + 1, size=B)
+    lens = np.asarray(lens, np.int32)
+    q = _random_bf16_rows(rng, B, H * G, D)
+    return q, kc, vc, ks, vs, bt, lens
+
+
+def _attention_reference(orc, mode, q, kc, vc, ks, vs, bt, lens, scale):
+    """The same attention from the gathered bf16 rows, with numpy/scipy in fp64."""
+    from scipy.special import softmax
+    B, HQ, D = q.shape
+    H = kc.shape[1]
+    G = HQ // H
+    ko, vo = orc.dequant_gather(mode, kc, vc, ks, vs, bt, lens)
+    kf, vf = _bits_to_f32(ko).astype(np.float64), _bits_to_f32(vo).astype(np.float64)
+    qf = _bits_to_f32(q).astype(np.float64)
+    off = np.concatenate([[0], np.cumsum(lens.astype(np.int64))])
+    out = np.zeros((B, HQ, D))
+    for b in range(B):
+        if lens[b] == 0:
+            continue
+        kb = np.repeat(kf[off[b]:off[b + 1]], G, axis=1)  # [L][HQ][D]: query head j -> kv head j // G
+        vb = np.repeat(vf[off[b]:off[b + 1]], G, axis=1)
+        w = softmax(scale * np.einsum("jd,ljd->jl", qf[b], kb), axis=1)
+        out[b] = np.einsum("jl,ljd->jd", w, vb)
+    return out, vf, off
+
+
+def pin_attention_against_library(orc):
+    """Against an independent fp64 formulation on the gathered rows, for every
+    scale mode, grouped heads, empty contexts and large scores."""
+    rng = np.random.default_rng(61)
+    for mode in (0, 1, 2):
+        for scale in (0.25, 40.0):
+            args = _attention_case(rng, mode=mode, lens=[0, 7, 20])
+            got = orc.paged_decode_attention(mode, *args, scale)
+            want, _, _ = _attention_reference(orc, mode, *args, scale)
+            assert np.all(np.isfinite(got))
+            assert np.allclose(got, want, rtol=1e-12, atol=1e-12), (mode, scale)
+            assert not got[0].any()  # empty context -> 0
+
+
+def pin_attention_closed_forms(orc):
+    """One position: the output is that position's V row.  Equal scores: the
+    output is the mean of the V rows."""
+    rng = np.random.default_rng(62)
+    q, kc, vc, ks, vs, bt, lens = _attention_case(rng, B=2, G=4, lens=[1, 9])
+    # sequence 1: every K code of kv head 0 equal, and one scale per position
+    # that is the same, so that all its scores are equal
+    for j in range(bt.shape[1]):
+        kc[bt[1, j], 0] = 5
+        ks[bt[1, j], 0] = np.float32(0.03)
+    out = orc.paged_decode_attention(0, q, kc, vc, ks, vs, bt, lens, 0.7)
+    _, vf, off = _attention_reference(orc, 0, q, kc, vc, ks, vs, bt, lens, 0.7)
+    for j in range(q.shape[1]):
+        h = j // 4
+        assert np.array_equal(out[0, j], vf[off[0], h])        # exact: weight 1
+    for j in range(4):                                          # kv head 0 of sequence 1
+        assert np.allclose(out[1, j], vf[off[1]:off[2], 0].mean(axis=0), rtol=1e-13, atol=1e-15)
+
+
 PINS = [pin_quantize_goldens, pin_dequant_goldens, pin_placement_golden,
         pin_exact_quantize_random, pin_exact_dequant_random, pin_invariants,
         pin_identity_table, pin_cumsum, pin_placement_bruteforce, pin_bounds_errors,
-        pin_bf16_placement_golden, pin_bf16_bruteforce, pin_per_block_reduces_to_per_channel]
+        pin_bf16_placement_golden, pin_bf16_bruteforce, pin_per_block_reduces_to_per_channel,
+        pin_attention_against_library, pin_attention_closed_forms]

@@ -48,6 +48,13 @@ MUTATIONS = [
                                        "float s = scale[(int64_t)(pos / block_size) * kv_heads + h];")]),
     ("per_row_scale_of_head_zero", [("float s = static_scale[t * kv_heads + h];",
                                      "float s = static_scale[t * kv_heads];")]),
+    ("attention_heads_interleaved", [("int h = j / group;", "int h = j % kv_heads;")]),
+    ("attention_without_max_shift", [("double w = exp(softmax_scale * dot - mx);",
+                                      "double w = exp(softmax_scale * dot);")]),
+    ("attention_keys_not_bf16", [("double kd = orc_bf16_to_f32(orc_dequantize_one(k_cache[row * head_dim + d], s));",
+                                  "double kd = (double)k_cache[row * head_dim + d] * s;")]),
+    ("attention_scale_dropped_in_weights", [("double w = exp(softmax_scale * dot - mx);",
+                                             "double w = exp(dot - mx);")]),
 ]
 
 
