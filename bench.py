@@ -53,7 +53,9 @@ KERNEL_SOURCES = ["dequant_kvc8_store_gb300/csrc/kvc8_store.cu",
                   "dequant_kvc8_store_gb300/csrc/kvc8_bf16.cu",
                   "dequant_kvc8_store_gb300/csrc/kvc8_internal.cuh"]
 PATH_TEXT = {"c8": "int8 cache", "bf16": "bf16 cache, no quantisation",
-             "fused": "int8 cache, store and gather fused into one append + gather launch"}
+             "fused": "int8 cache, store and gather fused into one append + gather launch",
+             "attention": "int8 cache, decode attention with the dequantisation fused in "
+                          "(one query per sequence, 4 query heads per kv head)"}
 WORKLOAD_TEXT = {
     "tiny": "tiny round trip: batch 2, q {5,19} after {3,0} cached, 2 kv heads x 64, block 16, "
             "8 blocks, dynamic scales",
@@ -196,7 +198,7 @@ def job_throughput(bytes_per_rank_step: int, world: int, step_ms_max: float) -> 
 def run_gpu(args, rank, world):
     import torch
     import dequant_kvc8_store_gb300 as kv
-    from dequant_kvc8_store_gb300.device import Bf16Batch, DeviceBatch
+    from dequant_kvc8_store_gb300.device import Bf16Batch, DecodeAttention, DeviceBatch
 
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
@@ -207,6 +209,8 @@ def run_gpu(args, rank, world):
         d = Bf16Batch(w, device=dev, seed=rank_seed(args.workload, rank))
     else:
         d = DeviceBatch(w, device=dev)
+    attn = (DecodeAttention(d, ATTN_GROUP, seed=rank_seed(args.workload, rank))
+            if args.path == "attention" else None)
     stream = torch.cuda.current_stream()
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     clean = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
@@ -217,7 +221,7 @@ def run_gpu(args, rank, world):
         # ends up holding clean lines (no write-back competes with the next op)
         flush.fill_(v)
         torch.sum(clean, dim=0, out=sink)
-    has_store = w.has_store and w.num_tokens > 0
+    has_store = w.has_store and w.num_tokens > 0 and attn is None
 
     def barrier():
         if world > 1:
@@ -226,18 +230,20 @@ def run_gpu(args, rank, world):
 
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
 
-    fused = args.path == "fused"
+    one_op = args.path in ("fused", "attention")  # no separate store op
 
     def step(e=None):
-        if not fused:
+        if not one_op:
             flush_l2(1)
         if e: e[0].record(stream)
-        if has_store and not fused:
+        if has_store and not one_op:
             d.store(stream)
         if e: e[1].record(stream)
         flush_l2(2)
         if e: e[2].record(stream)
-        if fused:
+        if attn is not None:
+            attn(stream)  # split plan + attention kernel + merge kernel
+        elif args.path == "fused":
             d.append_gather(stream)  # plan kernel + fused append/gather kernel
         else:
             d.gather(stream)  # plan kernel + gather kernel (programmatic dependent launch)
@@ -259,7 +265,7 @@ def run_gpu(args, rank, world):
             step(ev[i])
         barrier()
         wall = time.perf_counter() - t0
-    st_ms = [0.0 if fused else e[0].elapsed_time(e[1]) for e in ev]
+    st_ms = [0.0 if one_op else e[0].elapsed_time(e[1]) for e in ev]
     ga_ms = [e[2].elapsed_time(e[3]) for e in ev]
     step_ms = [a + b for a, b in zip(st_ms, ga_ms)]
     if d.error_code() != 0:
@@ -268,11 +274,11 @@ def run_gpu(args, rank, world):
              "gather_ms": float(np.mean(ga_ms)), "wall_s": wall}
     local["step_ms"], local["store_ms"], local["gather_ms"] = reduce_max(
         [local["step_ms"], local["store_ms"], local["gather_ms"]], device=dev)
-    e2e = run_e2e(args, w, d, dev, nbytes) if rank == 0 else None
+    e2e = run_e2e(args, w, d, dev, nbytes, attn) if rank == 0 else None
     return w, nbytes, local, clocks.summary(), e2e, has_store
 
 
-def run_e2e(args, w, d, dev, nbytes):
+def run_e2e(args, w, d, dev, nbytes, attn=None):
     """Same step through the public API with host buffers: H2D of the new K/V
     and the batch metadata from pinned memory, store, plan, gather, D2H of the
     gathered K/V into pinned memory -- all inside the timed region."""
@@ -289,16 +295,30 @@ def run_e2e(args, w, d, dev, nbytes):
         host["cu_q_lens"] = torch.from_numpy(w.cu_q_lens).pin_memory()
     host["context_kv_lens"] = torch.from_numpy(w.context_kv_lens).pin_memory()
     host["context_lengths"] = torch.from_numpy(w.context_lengths).pin_memory()
-    out_k = torch.empty(d.k_out.shape, dtype=torch.bfloat16).pin_memory()
-    out_v = torch.empty(d.v_out.shape, dtype=torch.bfloat16).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = out_k.numel() * 2 * 2
+    if attn is not None:  # the decode step: queries and metadata in, attention out
+        host = {"block_table": host["block_table"],
+                "context_lengths": host["context_lengths"]}
+        q_host = _bf16(attn.q_bits).pin_memory()
+        out_k = torch.empty(attn.out.shape, dtype=torch.bfloat16).pin_memory()
+        out_v = None
+        h2d = sum(t.numel() * t.element_size() for t in host.values()) + q_host.numel() * 2
+        d2h = out_k.numel() * 2
+    else:
+        out_k = torch.empty(d.k_out.shape, dtype=torch.bfloat16).pin_memory()
+        out_v = torch.empty(d.v_out.shape, dtype=torch.bfloat16).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = out_k.numel() * 2 * 2
     # bounded: at most ~16 GB of host<->device traffic, at least 3 steps
     steps = max(3, min(args.steps, 50, int(16e9 // max(1, h2d + d2h))))
 
     def step():
         for name, t in host.items():
             getattr(d, name).copy_(t, non_blocking=True)
+        if attn is not None:
+            attn.query.copy_(q_host, non_blocking=True)
+            attn(stream)
+            out_k.copy_(attn.out, non_blocking=True)
+            return
         if args.path == "fused":
             d.append_gather(stream)
         else:
@@ -363,6 +383,15 @@ def sub_workload(w: W.Workload, token_budget: int) -> W.Workload:
 
 def oracle_pass(w: W.Workload, path: str = "c8"):
     import oracle
+    if path == "attention":
+        rng = np.random.default_rng(7)
+        x = rng.standard_normal((w.num_seqs, w.kv_heads * ATTN_GROUP, w.head_dim)).astype(np.float32)
+        qb = (x.view(np.uint32) >> 16).astype(np.uint16)
+        t0 = time.perf_counter()
+        oracle.paged_decode_attention(w.quant_mode, qb, w.k_cache, w.v_cache, w.k_scale,
+                                      w.v_scale, w.block_table, w.context_lengths,
+                                      w.head_dim ** -0.5)
+        return time.perf_counter() - t0
     if path == "bf16":
         # a zero pool of the workload's shape: its prior bits do not change
         # what the copy costs
@@ -385,7 +414,12 @@ def oracle_pass(w: W.Workload, path: str = "c8"):
     return time.perf_counter() - t0
 
 
+ATTN_GROUP = 4  # 32 query heads on the 8 kv heads of the workloads
+
+
 def path_bytes(w: W.Workload, path: str) -> dict:
+    if path == "attention":
+        return W.algorithmic_bytes_attention(w, ATTN_GROUP)
     if path == "bf16":
         return W.algorithmic_bytes_bf16(w)
     if path == "fused":
@@ -459,7 +493,8 @@ def result_line(args, world, w, nbytes, t, clocks, e2e, has_store):
     total = nbytes["store"] + nbytes["gather"]
     value = job_throughput(total, world, t["step_ms"])
     fused = args.path == "fused"
-    timed_store = has_store and not fused and t["store_ms"] > 0
+    attention = args.path == "attention"
+    timed_store = has_store and not fused and not attention and t["store_ms"] > 0
     ops = {
         "store": {"ms": round(t["store_ms"], 5),
                   "GB_s": round(nbytes["store"] / (t["store_ms"] * 1e-3) / 1e9, 1) if timed_store else None,
@@ -471,6 +506,12 @@ def result_line(args, world, w, nbytes, t, clocks, e2e, has_store):
                            "tokens_per_s": round(w.total_context / (t["gather_ms"] * 1e-3), 1),
                            "bytes": nbytes["gather"]},
     }
+    if attention:  # one op: decode attention straight from the int8 cache
+        ops = {"decode_attention": {"ms": round(t["gather_ms"], 5),
+                                    "kernels": "split plan + attention + merge",
+                                    "GB_s": ops["dequant_gather"]["GB_s"],
+                                    "positions_per_s": ops["dequant_gather"]["tokens_per_s"],
+                                    "bytes": nbytes["gather"], "query_heads": ATTN_GROUP * w.kv_heads}}
     if fused:  # one op: the store is inside the fused launch
         ops["store"] = {"ms": 0.0, "GB_s": None, "tokens_per_s": None, "bytes": 0,
                         "note": "done inside the fused append + gather launch"}
@@ -481,11 +522,15 @@ def result_line(args, world, w, nbytes, t, clocks, e2e, has_store):
     dom_bytes = nbytes["gather"] if dom == "dequant_gather" else nbytes["store"]
     dom_ms = t["gather_ms"] if dom == "dequant_gather" else t["store_ms"]
     achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
+    if attention:
+        dom = "decode_attention"
     kname = "gather" if dom == "dequant_gather" else "store"
     if args.path == "bf16":
         kname += "_bf16"
     if fused:
         kname = "append_gather"
+    if attention:
+        kname = "attention"
     traffic = ncu_traffic(args.workload).get(kname + "_kernel")
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
@@ -497,14 +542,16 @@ def result_line(args, world, w, nbytes, t, clocks, e2e, has_store):
                    "path": PATH_TEXT[args.path],
                    "l2": "flushed before each timed op (256 MiB write, then 256 MiB read)",
                    "hbm_frac_of_step": round(total / (t["step_ms"] * 1e-3) / 1e9 / peak, 4),
-                   "tokens_per_s": {"store": ops["store"]["tokens_per_s"],
-                                    "dequant_gather": ops["dequant_gather"]["tokens_per_s"]}},
+                   "tokens_per_s": ({"decode_attention": ops["decode_attention"]["positions_per_s"]}
+                                    if attention else
+                                    {"store": ops["store"]["tokens_per_s"],
+                                     "dequant_gather": ops["dequant_gather"]["tokens_per_s"]})},
         "ops": ops,
         "roofline": {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "peak_kind": peak_kind, "traffic": traffic,
                      "algorithmic_bytes": dom_bytes},
-        "gpu_launches": args.steps * (3 if has_store and not fused else 2),
+        "gpu_launches": args.steps * (3 if (has_store and not fused) or attention else 2),
         "clocks": clocks,
         "e2e": e2e,
         "wall_s": round(t["wall_s"], 3),
@@ -521,9 +568,11 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["kvc8", "reference"], default="kvc8")
     ap.add_argument("--workload", choices=list(W.NAMED), default="prefill")
-    ap.add_argument("--path", choices=["c8", "bf16", "fused"], default="c8",
+    ap.add_argument("--path", choices=["c8", "bf16", "fused", "attention"], default="c8",
                     help="c8: the int8 cache (default); bf16: the cache without quantisation; "
-                         "fused: the int8 store and gather as one append + gather pass")
+                         "fused: the int8 store and gather as one append + gather pass; "
+                         "attention: decode attention (4 query heads per kv head) read "
+                         "straight from the int8 cache")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -12,5 +12,6 @@ from .binding import (DEV_BAD_BLOCK_ID, DEV_BAD_LENGTH, DEV_OK, DEV_OUT_ROW_RANG
                       kvc8_gather_workspace_bytes, NOALLOC_MAX_SEQS,
                       kvc8_get_error, kvc8_status_str, kvc8_store, kvc8_version, load,
                       kvc8_store_bf16, kvc8_gather_bf16, kvc8_append_gather,
-                      kvc8_build_append_metadata, kvc8_append_gather_planned)
+                      kvc8_build_append_metadata, kvc8_append_gather_planned,
+                      kvc8_attention_workspace_bytes, kvc8_paged_decode_attention)
 from .buildlib import build  # noqa: F401

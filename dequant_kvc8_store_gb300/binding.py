@@ -86,6 +86,11 @@ def configure(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.kvc8_store_bf16.restype = ctypes.c_int
     lib.kvc8_gather_bf16.argtypes = [G, P, P, P, P, P, P, P, i64, i64, i64, P, sz, P, P]
     lib.kvc8_gather_bf16.restype = ctypes.c_int
+    lib.kvc8_attention_workspace_bytes.argtypes = [G, i32]
+    lib.kvc8_attention_workspace_bytes.restype = sz
+    lib.kvc8_paged_decode_attention.argtypes = [G, i32, P, i64, i64, P, P, P, P, P, P,
+                                                ctypes.c_float, P, i64, i64, P, sz, P, P]
+    lib.kvc8_paged_decode_attention.restype = ctypes.c_int
     lib.kvc8_append_gather.argtypes = [G, i64, P, P, i64, i64, P, P, P, P, P, P, P, P, P, P, i64,
                                        i64, i64, P, sz, P, P]
     lib.kvc8_append_gather.restype = ctypes.c_int
@@ -275,6 +280,24 @@ def kvc8_append_gather_planned(g: Geom, num_tokens, key_states, value_states, x_
         int(out_rows), int(out_tok_stride), int(out_head_stride), _p(workspace),
         int(workspace_bytes), _p(dev_error), _stream(stream))
     _ok(st, "kvc8_append_gather_planned")
+
+
+def kvc8_attention_workspace_bytes(g: Geom, num_q_heads: int) -> int:
+    return int(load().kvc8_attention_workspace_bytes(ctypes.byref(g), int(num_q_heads)))
+
+
+def kvc8_paged_decode_attention(g: Geom, num_q_heads, query, q_seq_stride, q_head_stride,
+                                key_cache, value_cache, key_scale, value_scale, block_table,
+                                context_lengths, softmax_scale, out, out_seq_stride,
+                                out_head_stride, workspace, workspace_bytes, dev_error=None,
+                                stream=None) -> None:
+    st = load().kvc8_paged_decode_attention(
+        ctypes.byref(g), int(num_q_heads), _p(query), int(q_seq_stride), int(q_head_stride),
+        _p(key_cache), _p(value_cache), _p(key_scale), _p(value_scale), _p(block_table),
+        _p(context_lengths), float(softmax_scale), _p(out), int(out_seq_stride),
+        int(out_head_stride), _p(workspace), int(workspace_bytes), _p(dev_error),
+        _stream(stream))
+    _ok(st, "kvc8_paged_decode_attention")
 
 
 def kvc8_get_error(dev_error, reset: bool = False, stream=None) -> int:

@@ -19,7 +19,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(OUT_DIR, "libkvc8.so")
-SOURCES = ["kvc8_api.cu", "kvc8_store.cu", "kvc8_gather.cu", "kvc8_noalloc.cu", "kvc8_bf16.cu"]
+SOURCES = ["kvc8_api.cu", "kvc8_store.cu", "kvc8_gather.cu", "kvc8_noalloc.cu", "kvc8_bf16.cu",
+           "kvc8_attention.cu"]
 HEADERS = [os.path.join(CSRC, "kvc8_internal.cuh"), os.path.join(INCLUDE, "kvc8.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xptxas", "-v",

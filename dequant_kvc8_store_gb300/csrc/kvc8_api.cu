@@ -2,6 +2,7 @@
 // host-side argument checks, then the launches in kvc8_store.cu and
 // kvc8_gather.cu.  Nothing here allocates device memory or synchronises,
 // except kvc8_get_error, whose purpose is to synchronise.
+#include <cmath>
 #include <cstdint>
 
 #include "kvc8_internal.cuh"
@@ -344,6 +345,65 @@ kvc8_status kvc8_append_gather_planned(const kvc8_geom *g, int64_t num_tokens,
     if (st != KVC8_OK) return st;
     if (reset_plan_counter(workspace, stream) != cudaSuccess) return KVC8_ERR_CUDA;
     return cuda_status(launch_append_gather(a, p, /*use_pdl=*/false, stream));
+}
+
+size_t kvc8_attention_workspace_bytes(const kvc8_geom *g, int32_t num_q_heads) {
+    if (g == nullptr || g->num_seqs < 0 || g->kv_heads < 1 || num_q_heads < g->kv_heads) return 0;
+    return attention_workspace_bytes(*g, num_q_heads / g->kv_heads);
+}
+
+kvc8_status kvc8_paged_decode_attention(const kvc8_geom *g, int32_t num_q_heads,
+                                        const void *query, int64_t q_seq_stride,
+                                        int64_t q_head_stride, const int8_t *key_cache,
+                                        const int8_t *value_cache, const float *key_scale,
+                                        const float *value_scale, const int32_t *block_table,
+                                        const int32_t *context_lengths, float softmax_scale,
+                                        void *out, int64_t out_seq_stride,
+                                        int64_t out_head_stride, void *workspace,
+                                        size_t workspace_bytes, int32_t *dev_error,
+                                        cudaStream_t stream) {
+    kvc8_status st = check_geom(g);
+    if (st != KVC8_OK) return st;
+    if (num_q_heads < 1 || num_q_heads % g->kv_heads != 0) return KVC8_ERR_INVALID_ARG;
+    const int group = num_q_heads / g->kv_heads;
+    if (group > 8 || (g->head_dim != 64 && g->head_dim != 128) || g->block_size % 16 != 0)
+        return KVC8_ERR_UNSUPPORTED;
+    if (!std::isfinite(softmax_scale)) return KVC8_ERR_INVALID_ARG;
+    const int64_t splits =
+        ((int64_t)g->max_blocks_per_seq * g->block_size + kAttnChunk - 1) / kAttnChunk;
+    if ((int64_t)g->num_seqs * g->kv_heads * splits > (int64_t)INT32_MAX) return KVC8_ERR_UNSUPPORTED;
+    if (g->num_seqs == 0) return KVC8_OK;
+    if (query == nullptr || key_cache == nullptr || value_cache == nullptr ||
+        key_scale == nullptr || value_scale == nullptr || block_table == nullptr ||
+        context_lengths == nullptr || out == nullptr)
+        return KVC8_ERR_INVALID_ARG;
+    if (q_seq_stride < 0 || q_head_stride < 0 || q_seq_stride % 8 != 0 || q_head_stride % 8 != 0 ||
+        out_seq_stride < 0 || out_head_stride < 0)
+        return KVC8_ERR_INVALID_ARG;
+    if (!aligned(query, 16) || !aligned(key_cache, 16) || !aligned(value_cache, 16) ||
+        !aligned(key_scale, 16) || !aligned(value_scale, 16) || !aligned(out, 2))
+        return KVC8_ERR_INVALID_ARG;
+    if (workspace == nullptr || !aligned(workspace, kAlign) ||
+        workspace_bytes < attention_workspace_bytes(*g, group))
+        return KVC8_ERR_WORKSPACE;
+    AttnArgs a = {};
+    a.g = *g;
+    a.group = group;
+    a.q = static_cast<const uint16_t *>(query);
+    a.q_seq_stride = q_seq_stride;
+    a.q_head_stride = q_head_stride;
+    a.k_cache = key_cache;
+    a.v_cache = value_cache;
+    a.k_scale = key_scale;
+    a.v_scale = value_scale;
+    a.block_table = block_table;
+    a.context_lengths = context_lengths;
+    a.scale_log2 = (float)((double)softmax_scale * 1.4426950408889634);  // log2(e)
+    a.out = static_cast<uint16_t *>(out);
+    a.out_seq_stride = out_seq_stride;
+    a.out_head_stride = out_head_stride;
+    a.dev_error = dev_error;
+    return cuda_status(launch_attention(a, workspace, stream));
 }
 
 // Geometry checks for the bf16 cache (quant_mode is not used there).

@@ -205,6 +205,37 @@ struct AppendArgs {
 
 constexpr int kAppendRowsPerItem = 8;  // one (token, K|V, head) row per warp of a CTA
 
+// Paged decode attention over the int8 cache (kvc8_attention.cu).
+struct AttnArgs {
+    kvc8_geom g;
+    int32_t group;      // query heads per kv head (1..8)
+    int32_t chunk;      // positions per split (a multiple of 16)
+    const uint16_t *q;  // bf16 [B][H * group][D], strides below
+    int64_t q_seq_stride;
+    int64_t q_head_stride;
+    const int8_t *k_cache;
+    const int8_t *v_cache;
+    const float *k_scale;
+    const float *v_scale;
+    const int32_t *block_table;
+    const int32_t *context_lengths;
+    float scale_log2;  // softmax scale * log2(e)
+    uint16_t *out;     // bf16 [B][H * group][D], strides below
+    int64_t out_seq_stride;
+    int64_t out_head_stride;
+    const void *plan;  // the split plan (plan kernel with block_size = chunk)
+    float *part_o;     // [items][group][D] unnormalised partial outputs
+    float *part_m;     // [items][group] running maxima (log2 domain)
+    float *part_l;     // [items][group] running sums
+    int32_t *dev_error;
+};
+
+constexpr int kAttnChunk = 1024;  // positions per split of a sequence
+
+// Workspace of the attention: the split plan, then the partials.
+size_t attention_workspace_bytes(const kvc8_geom &g, int group);
+cudaError_t launch_attention(AttnArgs a, void *workspace, cudaStream_t stream);
+
 cudaError_t launch_store(const StoreArgs &a, cudaStream_t stream);
 cudaError_t launch_store_bf16(const StoreBf16Args &a, cudaStream_t stream);
 cudaError_t launch_gather_bf16(const GatherBf16Args &a, bool use_pdl, cudaStream_t stream);

@@ -201,3 +201,30 @@ class Bf16Batch:
 
     def error_code(self, reset=False) -> int:
         return B.kvc8_get_error(self.dev_error, reset=reset)
+
+
+class DecodeAttention:
+    """One decode query per sequence (num_q_heads = group * kv_heads, seeded
+    N(0, 1) bf16) attending over a DeviceBatch's int8 cache through
+    kvc8_paged_decode_attention; output bf16 [B][num_q_heads][D]."""
+
+    def __init__(self, d: DeviceBatch, group: int, seed: int = 0, softmax_scale=None):
+        self.d = d
+        w = d.w
+        self.num_q_heads = w.kv_heads * group
+        rng = np.random.default_rng([seed, 77])
+        x = rng.standard_normal((w.num_seqs, self.num_q_heads, w.head_dim)).astype(np.float32)
+        self.q_bits = (x.view(np.uint32) >> 16).astype(np.uint16)
+        self.query = _bf16(self.q_bits).to(d.device)
+        self.out = torch.empty_like(self.query)
+        self.scale = float(softmax_scale if softmax_scale is not None else w.head_dim ** -0.5)
+        self.ws_bytes = B.kvc8_attention_workspace_bytes(d.g, self.num_q_heads)
+        self.workspace = torch.empty(max(self.ws_bytes, 256), dtype=torch.uint8, device=d.device)
+
+    def __call__(self, stream=None):
+        d, q, o = self.d, self.query, self.out
+        B.kvc8_paged_decode_attention(d.g, self.num_q_heads, q, q.stride(0), q.stride(1),
+                                      d.k_cache, d.v_cache, d.k_scale, d.v_scale,
+                                      d.block_table, d.context_lengths, self.scale, o,
+                                      o.stride(0), o.stride(1), self.workspace, self.ws_bytes,
+                                      d.dev_error, stream)

@@ -348,3 +348,15 @@ def algorithmic_bytes_fused(w: Workload) -> dict:
     new = 2 * H * w.num_tokens
     total = new * (2 * D + D + per_row_scale + 2 * D) + cached * (D + per_row_scale + 2 * D)
     return {"store": 0, "gather": int(total + table)}
+
+
+def algorithmic_bytes_attention(w: Workload, group: int) -> dict:
+    """Algorithmic HBM bytes of one paged decode attention (int8 path): every
+    cached K and V code of every gathered position once, their scales, the
+    query read and the bf16 output written."""
+    H, D = w.kv_heads, w.head_dim
+    rows = 2 * H * w.total_context
+    scales = (rows * 4 if w.quant_mode == 0 else 2 * H * D * 4 if w.quant_mode == 1
+              else 4 * 2 * H * _blocks_touched(w, new_only=False))
+    q_out = 2 * w.num_seqs * H * group * D * 2
+    return {"store": 0, "gather": int(rows * D + scales + q_out)}

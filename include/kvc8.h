@@ -309,6 +309,53 @@ kvc8_status kvc8_append_gather_planned(const kvc8_geom *g, int64_t num_tokens,
                                        void *workspace, size_t workspace_bytes,
                                        int32_t *dev_error, cudaStream_t stream);
 
+/* Bytes of device workspace kvc8_paged_decode_attention needs for this
+ * geometry and number of query heads (a bound from num_seqs, kv_heads,
+ * max_blocks_per_seq * block_size and the group size).  Host function. */
+size_t kvc8_attention_workspace_bytes(const kvc8_geom *g, int32_t num_q_heads);
+
+/*
+ * kvc8_paged_decode_attention -- one decode query per sequence attends over its
+ * context in the int8 paged cache, reading the codes directly: the pages'
+ * MojoPagedDecodeGQA ("Mojo Opset" README, "Op List", Attention) on the
+ * values MojoDequantFromPagedKVCache ([PR379]) would produce, without writing
+ * them out.  The pages give no formula; the reading is grouped-query scaled
+ * dot-product attention: query head j (0 <= j < num_q_heads) uses kv head
+ * j / (num_q_heads / H), and
+ *   out[b][j] = sum_{p < context_lengths[b]} w_p * V'[b][p][h],
+ *   w = softmax_p(softmax_scale * <query[b][j], K'[b][p][h]>),
+ * with K', V' the bf16 rows kvc8_dequant_gather would write for those
+ * positions.  Computed with bf16 tensor-core products, fp32 accumulation,
+ * bf16-rounded softmax weights and a bf16 output (round to nearest even); an
+ * empty context gives zeros.  Enqueues a split plan, the attention kernel and
+ * a merge of the splits (programmatic dependent launches, no host sync).
+ *
+ *   num_q_heads     H * group with 1 <= group <= 8
+ *   query           bf16 [B][num_q_heads][D], element strides (q_seq_stride,
+ *                   q_head_stride, 1), multiples of 8, 16-byte aligned
+ *   caches, scales, block_table  as in kvc8_dequant_gather (all three modes)
+ *   context_lengths int32 [B], positions to attend per sequence
+ *   softmax_scale   finite, e.g. 1/sqrt(D)
+ *   out             bf16 [B][num_q_heads][D], strides (out_seq_stride,
+ *                   out_head_stride, 1)
+ *   workspace       >= kvc8_attention_workspace_bytes(g, num_q_heads) bytes,
+ *                   256-byte aligned; calls that overlap on the GPU need
+ *                   separate workspaces
+ * Supported: head_dim 64 or 128 and block_size a multiple of 16, else
+ * KVC8_ERR_UNSUPPORTED.  Block ids outside the pool are reported through
+ * dev_error and their 16-position pieces left out.
+ */
+kvc8_status kvc8_paged_decode_attention(const kvc8_geom *g, int32_t num_q_heads,
+                                        const void *query, int64_t q_seq_stride,
+                                        int64_t q_head_stride, const int8_t *key_cache,
+                                        const int8_t *value_cache, const float *key_scale,
+                                        const float *value_scale, const int32_t *block_table,
+                                        const int32_t *context_lengths, float softmax_scale,
+                                        void *out, int64_t out_seq_stride,
+                                        int64_t out_head_stride, void *workspace,
+                                        size_t workspace_bytes, int32_t *dev_error,
+                                        cudaStream_t stream);
+
 /*
  * kvc8_store_bf16 -- the same scatter as kvc8_store for a bf16 paged cache,
  * without quantisation: MojoStorePagedKVCache of the "Mojo Opset" README

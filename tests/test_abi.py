@@ -217,3 +217,32 @@ def test_build_append_metadata_rejects_bad_arguments():
                                           None, None) == kv.ERR_INVALID_ARG
     assert lib.kvc8_build_append_metadata(ctypes.byref(g), None, FAKE, None, None, FAKE, 8,
                                           None, None) == kv.ERR_WORKSPACE
+
+
+def test_attention_rejects_bad_arguments():
+    lib = kv.load()
+    g = kv.Geom(2, 8, 128, 16, 64, 8, 0)
+    ws_bytes = kv.kvc8_attention_workspace_bytes(g, 32)
+    assert ws_bytes > 0 and kv.kvc8_attention_workspace_bytes(g, 4) == 0
+
+    def call(g=g, hq=32, q=FAKE, qs=32 * 128, qh=128, scale=0.088, out=FAKE, ws=FAKE,
+             wsb=ws_bytes, **kw):
+        a = dict(kc=FAKE, vc=FAKE, ks=FAKE, vs=FAKE, bt=FAKE, lens=FAKE)
+        a.update(kw)
+        return lib.kvc8_paged_decode_attention(ctypes.byref(g), hq, q, qs, qh, a["kc"], a["vc"],
+                                               a["ks"], a["vs"], a["bt"], a["lens"], scale, out,
+                                               qs, qh, ws, wsb, None, None)
+    for name in ("kc", "vc", "ks", "vs", "bt", "lens"):
+        assert call(**{name: None}) == kv.ERR_INVALID_ARG, name
+    assert call(q=None) == kv.ERR_INVALID_ARG
+    assert call(out=None) == kv.ERR_INVALID_ARG
+    assert call(hq=30) == kv.ERR_INVALID_ARG           # not a multiple of the kv heads
+    assert call(hq=72) == kv.ERR_UNSUPPORTED            # group of 9
+    assert call(qs=100) == kv.ERR_INVALID_ARG
+    assert call(q=FAKE + 8) == kv.ERR_INVALID_ARG
+    assert call(scale=float("inf")) == kv.ERR_INVALID_ARG
+    assert call(ws=None) == kv.ERR_WORKSPACE
+    assert call(wsb=ws_bytes - 1) == kv.ERR_WORKSPACE
+    assert call(g=kv.Geom(2, 8, 96, 16, 64, 8, 0), qh=96, qs=32 * 96) == kv.ERR_UNSUPPORTED
+    assert call(g=kv.Geom(2, 8, 128, 8, 64, 8, 0)) == kv.ERR_UNSUPPORTED  # block of 8
+    assert call(g=kv.Geom(0, 8, 128, 16, 64, 8, 0), q=None) == kv.OK  # empty batch

@@ -13,22 +13,25 @@ KEYS = {"metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
         "roofline", "gpu_launches", "clocks", "e2e"}
 
 
-@pytest.mark.parametrize("path", ["c8", "bf16", "fused"])
+@pytest.mark.parametrize("path", ["c8", "bf16", "fused", "attention"])
 @pytest.mark.parametrize("gather_only", [False, True])
 def test_result_line_for_every_path(path, gather_only):
     w = W.tiny() if not gather_only else W.make_workload(
         "g", q_lens=[0, 0], ctx_before=[3, 17], kv_heads=2, head_dim=64, block_size=16,
         num_blocks=8, quant_mode=0, seed=1, gather_only=True)
     args = argparse.Namespace(path=path, workload="tiny", steps=7, warmup=3)
-    fused = path == "fused"
-    t = {"step_ms": 0.05, "store_ms": 0.0 if fused else 0.02, "gather_ms": 0.03, "wall_s": 1.0}
+    one_op = path in ("fused", "attention")
+    t = {"step_ms": 0.05, "store_ms": 0.0 if one_op else 0.02, "gather_ms": 0.03, "wall_s": 1.0}
     clocks = {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": [], "samples": 3}
     e2e = {"value": 1.0, "unit": "GB/s", "h2d_bytes_per_step": 1, "d2h_bytes_per_step": 1}
     line = bench.result_line(args, 1, w, bench.path_bytes(w, path), t, clocks, e2e,
-                             w.has_store and w.num_tokens > 0)
+                             w.has_store and w.num_tokens > 0 and path != "attention")
     assert KEYS <= set(line)
     json.dumps(line)
-    assert line["value"] > 0 and 0 < line["roofline"]["frac"]
-    assert line["gpu_launches"] == 7 * (2 if fused or gather_only else 3)
-    if fused:
+    assert line["value"] > 0 and line["roofline"]["achieved"] > 0
+    if path == "attention":
+        assert line["gpu_launches"] == 7 * 3 and "decode_attention" in line["ops"]
+    else:
+        assert line["gpu_launches"] == 7 * (2 if one_op or gather_only else 3)
+    if path == "fused":
         assert line["ops"]["store"]["ms"] == 0.0
