@@ -144,7 +144,10 @@ attention_kernel(const AttnArgs a) {
         const int b = seq_of_split(ts, B, tile);
         const int64_t j = tile - ts[b];
         const int nsplit = ts[b + 1] - ts[b];
-        const int64_t len = min((int64_t)ld_nc_s32(a.context_lengths + b), cap);
+        const int64_t raw_len = ld_nc_s32(a.context_lengths + b);
+        if (raw_len > cap && j == 0 && h == 0 && threadIdx.x == 0)
+            report(a.dev_error, KVC8_DEV_POS_BEYOND_TABLE);
+        const int64_t len = min(raw_len, cap);
         const int64_t p_begin = j * a.chunk;
         const int64_t p_end = min(len, p_begin + a.chunk);
 
