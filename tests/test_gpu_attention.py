@@ -118,7 +118,7 @@ def test_attention_small(i):
 
 def test_attention_strided_and_peaked():
     w = W.make_workload("attstr", q_lens=np.zeros(3, np.int64), ctx_before=[700, 2, 1500],
-                        kv_heads=4, head_dim=128, block_size=64, num_blocks=60, quant_mode=0,
+                        kv_heads=4, head_dim=128, block_size=64, num_blocks=80, quant_mode=0,
                         seed=310, with_store=False)
     rng = np.random.default_rng(410)
     for scale in (0.088, 3.0):  # 3.0: one position carries nearly all the weight
