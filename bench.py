@@ -70,6 +70,8 @@ WORKLOAD_TEXT = {
                "blocks, dynamic scales U[0.01,0.1]",
     "prefill_block": "prefill store+gather with per-block scales: the prefill batch shapes, "
                      "one static scale per (block, kv head) U[0.01,0.1]",
+    "decode_small": "decode batch cut to 64 sequences (profiling size): 1 new token, cached "
+                    "U[1,8192], 8 x 128, block 128, 4160-block pool, dynamic scales",
 }
 
 

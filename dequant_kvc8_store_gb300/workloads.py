@@ -290,8 +290,18 @@ def prefill_block(seed: int = 1005) -> Workload:
                          max_blocks_per_seq=32, quant_mode=2, seed=seed, outlier_channels=4)
 
 
+def decode_small(seed: int = 1006) -> Workload:
+    """The decode batch cut to 64 sequences (about 2 GB on the device): the
+    size for detailed profiles of the decode kernels."""
+    rng = np.random.default_rng([seed, 99])
+    ctx = rng.integers(1, 8192, size=64, endpoint=True)
+    return make_workload("decode_small", q_lens=np.ones(64, np.int64), ctx_before=ctx,
+                         kv_heads=8, head_dim=128, block_size=128, num_blocks=64 * 65,
+                         max_blocks_per_seq=65, quant_mode=0, seed=seed)
+
+
 NAMED = {"tiny": tiny, "prefill": prefill, "decode": decode, "mixed": mixed,
-         "longctx": longctx, "prefill_block": prefill_block}
+         "longctx": longctx, "prefill_block": prefill_block, "decode_small": decode_small}
 
 
 def algorithmic_bytes(w: Workload) -> dict:
