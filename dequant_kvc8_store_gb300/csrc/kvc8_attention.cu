@@ -66,10 +66,14 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return r;
 }
 
-// Code e (0..3) of a word of int8 codes as an exact float.
-__device__ __forceinline__ float code_f32(uint32_t w, int e) {
-    const uint32_t wb = w ^ 0x80808080u;  // c + 128 per byte
-    return __fsub_rn(__uint_as_float(__byte_perm(wb, 0x4B000000u, 0x7440 + e)), 8388736.0f);
+// Codes e0 and e1 of a word, times s0 and s1: two exact conversions and two
+// IEEE products, as packed fp32x2 operations.
+__device__ __forceinline__ float2 dequant2(uint32_t w, int e0, int e1, float s0, float s1) {
+    const uint32_t wb = w ^ 0x80808080u;
+    float2 x = make_float2(__uint_as_float(__byte_perm(wb, 0x4B000000u, 0x7440 + e0)),
+                           __uint_as_float(__byte_perm(wb, 0x4B000000u, 0x7440 + e1)));
+    x = __fadd2_rn(x, make_float2(-8388736.0f, -8388736.0f));  // exact: c
+    return __fmul2_rn(x, make_float2(s0, s1));
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t x) { return __uint_as_float(x << 16); }
@@ -99,6 +103,142 @@ __device__ __forceinline__ void load_bytes(const void *p, uint32_t *w) {
     }
 }
 
+// The codes, scales and masks of one 16-position sub-tile, as one thread of
+// the warp holds them.
+template <int D>
+struct Tile {
+    uint32_t k0[D / 16], k1[D / 16];  // K codes: positions gid, gid + 8; bytes [tig*D/4, +D/4)
+    uint32_t v[4][D / 32];            // V codes: positions 2tig, 2tig+1, 2tig+8, 2tig+9
+    float sk0, sk1, sv[4];            // modes 0 and 2: the rows' (or block's) scales
+    int32_t valid;                    // positions of the sub-tile before the context end
+    bool ok;                          // the block id is inside the pool
+};
+
+template <int MODE, int D>
+__device__ __forceinline__ void load_tile(const AttnArgs &a, int b, int h, int64_t p0,
+                                          int64_t p_end, int gid, int tig, int lane,
+                                          Tile<D> &t) {
+    constexpr int KB = D / 4, VB = D / 8;
+    const int H = a.g.kv_heads, bs = a.g.block_size, MB = a.g.max_blocks_per_seq;
+    const int64_t lb = (int64_t)((uint32_t)p0 / (uint32_t)bs);
+    const int32_t blk = ld_nc_s32(a.block_table + (int64_t)b * MB + lb);
+    t.ok = blk >= 0 && blk < a.g.num_blocks;
+    t.valid = (int32_t)min((int64_t)kSub, p_end - p0);
+    if (!t.ok) {
+        if (lane == 0) report(a.dev_error, KVC8_DEV_BAD_BLOCK_ID);
+        return;
+    }
+    const int64_t row0 = ((int64_t)blk * H + h) * bs + (p0 - lb * bs);
+    const int8_t *kp = a.k_cache + (row0 + gid) * D + tig * KB;
+    load_bytes<KB>(kp, t.k0);
+    load_bytes<KB>(kp + 8 * D, t.k1);
+    const int8_t *vp = a.v_cache + (row0 + 2 * tig) * D + gid * VB;
+    load_bytes<VB>(vp, t.v[0]);
+    load_bytes<VB>(vp + D, t.v[1]);
+    load_bytes<VB>(vp + 8 * D, t.v[2]);
+    load_bytes<VB>(vp + 9 * D, t.v[3]);
+    if (MODE == 0) {
+        t.sk0 = ld_nc_f32(a.k_scale + row0 + gid);
+        t.sk1 = ld_nc_f32(a.k_scale + row0 + gid + 8);
+        t.sv[0] = ld_nc_f32(a.v_scale + row0 + 2 * tig);
+        t.sv[1] = ld_nc_f32(a.v_scale + row0 + 2 * tig + 1);
+        t.sv[2] = ld_nc_f32(a.v_scale + row0 + 2 * tig + 8);
+        t.sv[3] = ld_nc_f32(a.v_scale + row0 + 2 * tig + 9);
+    } else if (MODE == 2) {
+        t.sk0 = t.sk1 = ld_nc_f32(a.k_scale + (int64_t)blk * H + h);
+        t.sv[0] = t.sv[1] = t.sv[2] = t.sv[3] = ld_nc_f32(a.v_scale + (int64_t)blk * H + h);
+    }
+}
+
+// O^T += V'^T P^T for one sub-tile; MASK zeroes V' rows at or past `valid`.
+template <int MODE, int D, bool MASK>
+__device__ __forceinline__ void pv_tile(const float *s_tab_v, const Tile<D> &t, int gid, int tig,
+                                        uint32_t pb0, uint32_t pb1, float (*o)[4]) {
+    constexpr int VB = D / 8, KS = D / 16;
+    bool vv[4] = {true, true, true, true};
+    if (MASK) {
+        vv[0] = 2 * tig < t.valid;
+        vv[1] = 2 * tig + 1 < t.valid;
+        vv[2] = 2 * tig + 8 < t.valid;
+        vv[3] = 2 * tig + 9 < t.valid;
+    }
+#pragma unroll
+    for (int i = 0; i < KS; ++i) {
+        float sd0 = 0.0f, sd1 = 0.0f;
+        if (MODE == 1) {
+            const float2 t2 = *reinterpret_cast<const float2 *>(s_tab_v + gid * VB + 2 * i);
+            sd0 = t2.x;
+            sd1 = t2.y;
+        }
+        float f[4][2];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 x = dequant2(t.v[e][(2 * i) >> 2], (2 * i) & 3, (2 * i + 1) & 3,
+                                      MODE == 1 ? sd0 : t.sv[e], MODE == 1 ? sd1 : t.sv[e]);
+            f[e][0] = x.x;
+            f[e][1] = x.y;
+            if (MASK && !vv[e]) f[e][0] = f[e][1] = 0.0f;
+        }
+        mma_bf16(o[i], pack_bf16(f[0][0], f[1][0]), pack_bf16(f[0][1], f[1][1]),
+                 pack_bf16(f[2][0], f[3][0]), pack_bf16(f[2][1], f[3][1]), pb0, pb1);
+    }
+}
+
+template <int MODE, int D>
+__device__ __forceinline__ void compute_tile(const AttnArgs &a, int h, const float *s_tab,
+                                             const uint32_t *qf, int gid, int tig,
+                                             const Tile<D> &t, float &m0, float &m1, float &l0,
+                                             float &l1, float (*o)[4]) {
+    constexpr int KB = D / 4, KS = D / 16;
+    const int H = a.g.kv_heads;
+    // S^T = K' Q^T
+    float c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+    for (int kk = 0; kk < KS; ++kk) {
+        float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        if (MODE == 1) {
+            const float4 t4 = *reinterpret_cast<const float4 *>(s_tab + h * D + tig * KB + 4 * kk);
+            s4[0] = t4.x; s4[1] = t4.y; s4[2] = t4.z; s4[3] = t4.w;
+        }
+        const float2 a01 = dequant2(t.k0[kk], 0, 1, MODE == 1 ? s4[0] : t.sk0, MODE == 1 ? s4[1] : t.sk0);
+        const float2 a23 = dequant2(t.k0[kk], 2, 3, MODE == 1 ? s4[2] : t.sk0, MODE == 1 ? s4[3] : t.sk0);
+        const float2 b01 = dequant2(t.k1[kk], 0, 1, MODE == 1 ? s4[0] : t.sk1, MODE == 1 ? s4[1] : t.sk1);
+        const float2 b23 = dequant2(t.k1[kk], 2, 3, MODE == 1 ? s4[2] : t.sk1, MODE == 1 ? s4[3] : t.sk1);
+        mma_bf16(c, pack_bf16(a01.x, a01.y), pack_bf16(b01.x, b01.y), pack_bf16(a23.x, a23.y),
+                 pack_bf16(b23.x, b23.y), qf[2 * kk], qf[2 * kk + 1]);
+    }
+    // scale into the log2 domain, mask positions past the context
+    const bool va = gid < t.valid, vb8 = gid + 8 < t.valid;
+    c[0] = va ? c[0] * a.scale_log2 : -INFINITY;
+    c[1] = va ? c[1] * a.scale_log2 : -INFINITY;
+    c[2] = vb8 ? c[2] * a.scale_log2 : -INFINITY;
+    c[3] = vb8 ? c[3] * a.scale_log2 : -INFINITY;
+    // online softmax per query head (a column: lanes with the same tig)
+    float x0 = fmaxf(c[0], c[2]), x1 = fmaxf(c[1], c[3]);
+#pragma unroll
+    for (int sh = 4; sh < 32; sh <<= 1) {
+        x0 = fmaxf(x0, __shfl_xor_sync(0xFFFFFFFFu, x0, sh));
+        x1 = fmaxf(x1, __shfl_xor_sync(0xFFFFFFFFu, x1, sh));
+    }
+    const float n0 = fmaxf(m0, x0), n1 = fmaxf(m1, x1);  // finite: valid >= 1
+    const float corr0 = exp2f(m0 - n0), corr1 = exp2f(m1 - n1);
+    m0 = n0;
+    m1 = n1;
+    const uint32_t plo = pack_bf16(exp2f(c[0] - n0), exp2f(c[1] - n1));  // position gid
+    const uint32_t phi = pack_bf16(exp2f(c[2] - n0), exp2f(c[3] - n1));  // position gid+8
+    l0 = l0 * corr0 + (bf16_lo(plo) + bf16_lo(phi));
+    l1 = l1 * corr1 + (bf16_hi(plo) + bf16_hi(phi));
+#pragma unroll
+    for (int i = 0; i < KS; ++i) {
+        o[i][0] *= corr0; o[i][2] *= corr0;
+        o[i][1] *= corr1; o[i][3] *= corr1;
+    }
+    const uint32_t pb0 = transpose8x8(plo), pb1 = transpose8x8(phi);
+    const float *s_tab_v = s_tab + (H + h) * D;
+    if (t.valid == kSub) pv_tile<MODE, D, false>(s_tab_v, t, gid, tig, pb0, pb1, o);
+    else pv_tile<MODE, D, true>(s_tab_v, t, gid, tig, pb0, pb1, o);
+}
+
 // One work item = (split j of sequence b, kv head h).
 template <int MODE, int D>
 __global__ void __launch_bounds__(kAttnThreads)
@@ -107,7 +247,7 @@ attention_kernel(const AttnArgs a) {
     constexpr int VB = D / 8;   // V code bytes per thread per position
     constexpr int KS = D / 16;  // QK k-steps = PV m-tiles
     const int H = a.g.kv_heads, bs = a.g.block_size, B = a.g.num_seqs;
-    const int MB = a.g.max_blocks_per_seq, NB = a.g.num_blocks;
+    const int MB = a.g.max_blocks_per_seq;
     const int G = a.group;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int gid = lane >> 2, tig = lane & 3;
@@ -169,108 +309,14 @@ attention_kernel(const AttnArgs a) {
 #pragma unroll
         for (int i = 0; i < KS; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.0f;
 
-        for (int64_t p0 = p_begin + warp * kSub; p0 < p_end; p0 += kAttnWarps * kSub) {
-            const int64_t lb = (int64_t)((uint32_t)p0 / (uint32_t)bs);
-            const int32_t blk = ld_nc_s32(a.block_table + (int64_t)b * MB + lb);
-            if (blk < 0 || blk >= NB) {
-                if (lane == 0) report(a.dev_error, KVC8_DEV_BAD_BLOCK_ID);
-                continue;
-            }
-            const int64_t row0 = ((int64_t)blk * H + h) * bs + (p0 - lb * bs);
-            // K codes: positions gid and gid + 8, bytes [tig*KB, +KB)
-            uint32_t k0[KB / 4], k1[KB / 4];
-            const int8_t *kp = a.k_cache + (row0 + gid) * D + tig * KB;
-            load_bytes<KB>(kp, k0);
-            load_bytes<KB>(kp + 8 * D, k1);
-            // V codes: positions 2tig, 2tig+1, 2tig+8, 2tig+9, bytes [gid*VB, +VB)
-            uint32_t v[4][VB / 4];
-            const int8_t *vp = a.v_cache + (row0 + 2 * tig) * D + gid * VB;
-            load_bytes<VB>(vp, v[0]);
-            load_bytes<VB>(vp + D, v[1]);
-            load_bytes<VB>(vp + 8 * D, v[2]);
-            load_bytes<VB>(vp + 9 * D, v[3]);
-            float sk0 = 0.0f, sk1 = 0.0f, sv[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-            if (MODE == 0) {
-                sk0 = ld_nc_f32(a.k_scale + row0 + gid);
-                sk1 = ld_nc_f32(a.k_scale + row0 + gid + 8);
-                sv[0] = ld_nc_f32(a.v_scale + row0 + 2 * tig);
-                sv[1] = ld_nc_f32(a.v_scale + row0 + 2 * tig + 1);
-                sv[2] = ld_nc_f32(a.v_scale + row0 + 2 * tig + 8);
-                sv[3] = ld_nc_f32(a.v_scale + row0 + 2 * tig + 9);
-            } else if (MODE == 2) {
-                sk0 = sk1 = ld_nc_f32(a.k_scale + (int64_t)blk * H + h);
-                sv[0] = sv[1] = sv[2] = sv[3] = ld_nc_f32(a.v_scale + (int64_t)blk * H + h);
-            }
-            const bool va = p0 + gid < p_end, vb8 = p0 + gid + 8 < p_end;
-
-            // S^T = K' Q^T
-            float c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-            for (int kk = 0; kk < KS; ++kk) {
-                float s4[4];
-                if (MODE == 1) {
-                    const float4 t4 = *reinterpret_cast<const float4 *>(s_tab + h * D + tig * KB + 4 * kk);
-                    s4[0] = t4.x; s4[1] = t4.y; s4[2] = t4.z; s4[3] = t4.w;
-                }
-                float f0[4], f1[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    f0[e] = __fmul_rn(code_f32(k0[kk], e), MODE == 1 ? s4[e] : sk0);
-                    f1[e] = __fmul_rn(code_f32(k1[kk], e), MODE == 1 ? s4[e] : sk1);
-                }
-                mma_bf16(c, pack_bf16(f0[0], f0[1]), pack_bf16(f1[0], f1[1]),
-                         pack_bf16(f0[2], f0[3]), pack_bf16(f1[2], f1[3]), qf[2 * kk],
-                         qf[2 * kk + 1]);
-            }
-            // scale into the log2 domain, mask positions past the context
-            c[0] = va ? c[0] * a.scale_log2 : -INFINITY;
-            c[1] = va ? c[1] * a.scale_log2 : -INFINITY;
-            c[2] = vb8 ? c[2] * a.scale_log2 : -INFINITY;
-            c[3] = vb8 ? c[3] * a.scale_log2 : -INFINITY;
-            // online softmax per query head (a column: lanes with the same tig)
-            float x0 = fmaxf(c[0], c[2]), x1 = fmaxf(c[1], c[3]);
-#pragma unroll
-            for (int sh = 4; sh < 32; sh <<= 1) {
-                x0 = fmaxf(x0, __shfl_xor_sync(0xFFFFFFFFu, x0, sh));
-                x1 = fmaxf(x1, __shfl_xor_sync(0xFFFFFFFFu, x1, sh));
-            }
-            const float n0 = fmaxf(m0, x0), n1 = fmaxf(m1, x1);  // finite: p0 < p_end
-            const float corr0 = exp2f(m0 - n0), corr1 = exp2f(m1 - n1);
-            m0 = n0;
-            m1 = n1;
-            const uint32_t plo = pack_bf16(exp2f(c[0] - n0), exp2f(c[1] - n1));  // position gid
-            const uint32_t phi = pack_bf16(exp2f(c[2] - n0), exp2f(c[3] - n1));  // position gid+8
-            l0 = l0 * corr0 + (bf16_lo(plo) + bf16_lo(phi));
-            l1 = l1 * corr1 + (bf16_hi(plo) + bf16_hi(phi));
-#pragma unroll
-            for (int i = 0; i < KS; ++i) {
-                o[i][0] *= corr0; o[i][2] *= corr0;
-                o[i][1] *= corr1; o[i][3] *= corr1;
-            }
-            const uint32_t pb0 = transpose8x8(plo), pb1 = transpose8x8(phi);
-            // O^T += V'^T P^T; V' of positions past the context is zero
-            const bool vv[4] = {p0 + 2 * tig < p_end, p0 + 2 * tig + 1 < p_end,
-                                p0 + 2 * tig + 8 < p_end, p0 + 2 * tig + 9 < p_end};
-#pragma unroll
-            for (int i = 0; i < KS; ++i) {
-                float sd0 = 0.0f, sd1 = 0.0f;
-                if (MODE == 1) {
-                    const float2 t2 = *reinterpret_cast<const float2 *>(s_tab + (H + h) * D + gid * VB + 2 * i);
-                    sd0 = t2.x;
-                    sd1 = t2.y;
-                }
-                float f[4][2];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const uint32_t w = v[e][(2 * i) >> 2];
-                    const float lo = __fmul_rn(code_f32(w, (2 * i) & 3), MODE == 1 ? sd0 : sv[e]);
-                    const float hi = __fmul_rn(code_f32(w, (2 * i + 1) & 3), MODE == 1 ? sd1 : sv[e]);
-                    f[e][0] = vv[e] ? lo : 0.0f;
-                    f[e][1] = vv[e] ? hi : 0.0f;
-                }
-                mma_bf16(o[i], pack_bf16(f[0][0], f[1][0]), pack_bf16(f[0][1], f[1][1]),
-                         pack_bf16(f[2][0], f[3][0]), pack_bf16(f[2][1], f[3][1]), pb0, pb1);
-            }
+        // One sub-tile at a time: requesting the next one before computing the
+        // current (a register double buffer) measured slower, the extra
+        // registers costing more occupancy than the overlap gained.
+        constexpr int64_t kStride = kAttnWarps * kSub;
+        for (int64_t p0 = p_begin + warp * kSub; p0 < p_end; p0 += kStride) {
+            Tile<D> t;
+            load_tile<MODE, D>(a, b, h, p0, p_end, gid, tig, lane, t);
+            if (t.ok) compute_tile<MODE, D>(a, h, s_tab, qf, gid, tig, t, m0, m1, l0, l1, o);
         }
         // row sums over the warp's positions
 #pragma unroll
@@ -327,34 +373,66 @@ attention_kernel(const AttnArgs a) {
 }
 
 // Sequences with more than one split: combine the splits' partials; empty
-// sequences: zeros.  One CTA per (sequence, kv head).
+// sequences: zeros.  One CTA per (sequence, kv head); a warp per query head,
+// the lanes over channels (D/32 each), the split weights computed 32 at a
+// time and broadcast by shuffles.
 __global__ void __launch_bounds__(kMergeThreads)
 attention_merge_kernel(const AttnArgs a) {
     pdl_wait_prior_grid();  // all partials are written
     const int H = a.g.kv_heads, B = a.g.num_seqs, D = a.g.head_dim, G = a.group;
     const int b = blockIdx.x / H, h = blockIdx.x - b * H;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int32_t *ts = reinterpret_cast<const int32_t *>(static_cast<const char *>(a.plan) +
                                                           plan_tile_start_at(B));
     const int first = ts[b], nsplit = ts[b + 1] - ts[b];
     if (nsplit == 1) return;
-    for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
-        const int hd = idx / D, d = idx - hd * D;
-        float r = 0.0f;
+    const int per = D / 32;  // channels per lane: 2 or 4
+    for (int hd = warp; hd < G; hd += kMergeThreads / 32) {
+        uint16_t *dst = a.out + (int64_t)b * a.out_seq_stride +
+                        (int64_t)(h * G + hd) * a.out_head_stride + lane * per;
+        float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
         if (nsplit > 1) {
             float M = -INFINITY;
-            for (int j = 0; j < nsplit; ++j)
+            for (int j = lane; j < nsplit; j += 32)
                 M = fmaxf(M, a.part_m[((int64_t)(first + j) * H + h) * G + hd]);
-            float L = 0.0f, O = 0.0f;
-            for (int j = 0; j < nsplit; ++j) {
-                const int64_t it = (int64_t)(first + j) * H + h;
-                const float f = exp2f(a.part_m[it * G + hd] - M);
-                L += a.part_l[it * G + hd] * f;
-                O += a.part_o[(it * G + hd) * D + d] * f;
+#pragma unroll
+            for (int sh = 16; sh > 0; sh >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, sh));
+            float L = 0.0f;
+            for (int j0 = 0; j0 < nsplit; j0 += 32) {
+                const int j = j0 + lane;
+                float f = 0.0f;
+                if (j < nsplit) {
+                    const int64_t it = ((int64_t)(first + j) * H + h) * G + hd;
+                    f = exp2f(a.part_m[it] - M);
+                    L += a.part_l[it] * f;
+                }
+                const int n = min(32, nsplit - j0);
+                for (int k = 0; k < n; ++k) {
+                    const float fk = __shfl_sync(0xFFFFFFFFu, f, k);
+                    const float *po = a.part_o + (((int64_t)(first + j0 + k) * H + h) * G + hd) * D +
+                                      lane * per;
+                    if (per == 4) {
+                        const float4 v = *reinterpret_cast<const float4 *>(po);
+                        acc[0] += fk * v.x; acc[1] += fk * v.y; acc[2] += fk * v.z; acc[3] += fk * v.w;
+                    } else {
+                        const float2 v = *reinterpret_cast<const float2 *>(po);
+                        acc[0] += fk * v.x; acc[1] += fk * v.y;
+                    }
+                }
             }
-            r = O / L;
+#pragma unroll
+            for (int sh = 16; sh > 0; sh >>= 1) L += __shfl_xor_sync(0xFFFFFFFFu, L, sh);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[e] /= L;
         }
-        a.out[(int64_t)b * a.out_seq_stride + (int64_t)(h * G + hd) * a.out_head_stride + d] =
-            (uint16_t)(pack_bf16(r, 0.0f) & 0xFFFFu);
+#pragma unroll
+        for (int e = 0; e < 4; e += 2) {
+            if (e < per) {
+                const uint32_t pr = pack_bf16(acc[e], acc[e + 1]);
+                dst[e] = (uint16_t)(pr & 0xFFFFu);
+                dst[e + 1] = (uint16_t)(pr >> 16);
+            }
+        }
     }
 }
 

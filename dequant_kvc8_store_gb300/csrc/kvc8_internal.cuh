@@ -230,7 +230,7 @@ struct AttnArgs {
     int32_t *dev_error;
 };
 
-constexpr int kAttnChunk = 1024;  // positions per split of a sequence
+constexpr int kAttnChunk = 2048;  // positions per split of a sequence
 
 // Workspace of the attention: the split plan, then the partials.
 size_t attention_workspace_bytes(const kvc8_geom &g, int group);

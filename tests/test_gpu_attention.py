@@ -90,7 +90,7 @@ def check_attention(w, group, scale, qb, got, seqs=None):
 
 
 CASES = [
-    # lens cross 16-position pieces, blocks and the 1024-position splits
+    # lens cross 16-position pieces, blocks and the 2048-position splits
     dict(lens=[0, 1, 15, 16, 300], H=2, G=4, D=128, bs=16, mode=0),
     dict(lens=[3000, 1, 1024, 1025, 2048], H=4, G=8, D=64, bs=32, mode=0),
     dict(lens=[77, 513, 1], H=2, G=1, D=128, bs=64, mode=1),
