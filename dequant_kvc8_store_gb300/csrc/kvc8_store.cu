@@ -76,6 +76,28 @@ __device__ __forceinline__ uint32_t pack_lo_bytes(uint32_t a, uint32_t b, uint32
     return __byte_perm(__byte_perm(a, b, 0x0040), __byte_perm(c, d, 0x0040), 0x5410);
 }
 
+// The groups of four codes flagged in `fix` (bit q: codes 4q..4q+3 of a
+// lane's run), recomputed from the source values one by one with the exact
+// fallback and stored over the fast codes at dst.  Mode 1 reads each value's
+// scale and reciprocal; modes 0 and 2 use the row's.
+template <int MODE>
+__device__ __noinline__ void fix_codes(const uint16_t *src, int8_t *dst, uint32_t fix, float s_row,
+                                       float r_row, const float *st, const float *rt) {
+    while (fix != 0u) {
+        const int q = __ffs(fix) - 1;
+        fix &= fix - 1u;
+        uint32_t c4[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int j = 4 * q + e;
+            const float x = __uint_as_float((uint32_t)src[j] << 16);
+            const int code = MODE == 1 ? quant_one(x, ld_nc_f32(st + j), rt[j]) : quant_one(x, s_row, r_row);
+            c4[e] = (uint32_t)code;
+        }
+        *reinterpret_cast<uint32_t *>(dst + 4 * q) = pack_lo_bytes(c4[0], c4[1], c4[2], c4[3]);
+    }
+}
+
 template <bool V32>
 __device__ __forceinline__ void load32(const uint16_t *p, uint32_t w[8]) {
     if (V32) {
@@ -283,6 +305,7 @@ store_kernel(const StoreArgs a) {
                 const float *st = (kv ? a.v_scale : a.k_scale) + (int64_t)h * D + c * E;  // static mode
 
                 uint32_t cw[W / 2];  // packed codes, four per word
+                uint32_t fix = 0u;   // bit q: codes 4q..4q+3 need the exact path
                 const bool force_exact = (MODE == 1) ? !all_fast : (r_row == 0.0f);
                 // Dynamic mode: r_lo <= r (1 - 2^-23) and r_hi >= r (1 + 2^-23)
                 // bracket every value fl(x / s) can take, so when x r_lo and
@@ -320,23 +343,11 @@ store_kernel(const StoreArgs a) {
                         mbits[2 * e] = __float_as_uint(m2.x);  // low byte = code
                         mbits[2 * e + 1] = __float_as_uint(m2.y);
                     }
-                    uint32_t word = pack_lo_bytes(mbits[0], mbits[1], mbits[2], mbits[3]);
+                    cw[i / 2] = pack_lo_bytes(mbits[0], mbits[1], mbits[2], mbits[3]);
                     const bool near = (MODE == 0) ? (differ != 0u) : (dm >= kNearTie);
-                    if ((near || force_exact) && on) {
-                        // rare: recompute these four codes one by one, exact where needed
-                        int q[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const uint32_t wi = w[k][i + (e >> 1)];
-                            const float x = __uint_as_float((e & 1) ? (wi & 0xFFFF0000u) : (wi << 16));
-                            const int j = 2 * i + e;
-                            q[e] = MODE == 1 ? quant_one(x, ld_nc_f32(st + j), rt[j])
-                                             : quant_one(x, s_row, r_row);
-                        }
-                        word = pack_lo_bytes((uint32_t)q[0], (uint32_t)q[1], (uint32_t)q[2], (uint32_t)q[3]);
-                    }
-                    cw[i / 2] = word;
+                    fix |= near ? (1u << (i / 2)) : 0u;
                 }
+                if (force_exact) fix = (1u << (W / 2)) - 1u;
                 if (on) {
                     int8_t *cache = kv ? a.v_cache : a.k_cache;
                     const int64_t dst_row = ((int64_t)blk * H + h) * bs + slot;
@@ -344,6 +355,13 @@ store_kernel(const StoreArgs a) {
                     if (E == 32) store_codes32<V32>(dst, cw);
                     else store_codes16(dst, cw);
                     if (MODE == 0 && c == 0) (kv ? a.v_scale : a.k_scale)[dst_row] = s_row;
+                    if (fix != 0u) {
+                        // rare: the flagged groups of four codes again, one by one,
+                        // exact where needed, over the fast codes just stored
+                        const uint16_t *src = (kv ? a.v_states : a.k_states) + t * a.x_tok_stride +
+                                              (int64_t)h * a.x_head_stride + c * E;
+                        fix_codes<MODE>(src, dst, fix, s_row, r_row, st, rt);
+                    }
                 }
             }
         }
