@@ -139,7 +139,7 @@ __device__ __forceinline__ void store_codes16(int8_t *p, const uint32_t c[4]) {
 // per channel / 2 static per block,
 // V32: 32-byte aligned rows (256-bit loads and stores).
 template <int E, int LANES, int MODE, bool V32>
-__global__ void __launch_bounds__(kWarpsPerCta * 32, 3)
+__global__ void __launch_bounds__(kWarpsPerCta * 32, MODE == 0 ? 3 : 4)
 store_kernel(const StoreArgs a) {
     constexpr int W = E / 2;                  // bf16x2 words per lane per row
     constexpr int RPP = 32 / LANES;           // rows per warp pass
