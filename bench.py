@@ -51,6 +51,7 @@ METRIC = "achieved HBM GB/s (% of ~8 TB/s) and K+V tokens/s for store and dequan
 KERNEL_SOURCES = ["dequant_kvc8_store_gb300/csrc/kvc8_store.cu",
                   "dequant_kvc8_store_gb300/csrc/kvc8_gather.cu",
                   "dequant_kvc8_store_gb300/csrc/kvc8_bf16.cu",
+                  "dequant_kvc8_store_gb300/csrc/kvc8_attention.cu",
                   "dequant_kvc8_store_gb300/csrc/kvc8_internal.cuh"]
 PATH_TEXT = {"c8": "int8 cache", "bf16": "bf16 cache, no quantisation",
              "fused": "int8 cache, store and gather fused into one append + gather launch",
