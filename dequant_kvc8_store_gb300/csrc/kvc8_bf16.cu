@@ -28,19 +28,19 @@ __device__ __forceinline__ Slot token_slot(const StoreBf16Args &a, int64_t t, in
     const int bs = a.g.block_size;
     Slot r{0, 0, 0};
     int b;
-    int64_t i_in_seq;
+    int64_t i_in_seq, ctx;
     bool bad_len = false;
     if (a.cu_q_lens != nullptr) {
-        b = seq_of_token(a.cu_q_lens, B, t, lane);
-        const int64_t first = ld_nc_s32(a.cu_q_lens + b);
-        const int64_t next = ld_nc_s32(a.cu_q_lens + b + 1);
-        i_in_seq = t - first;
-        bad_len = !(first <= t && t < next);
+        const TokenSeq ts = seq_ctx_of_token(a.cu_q_lens, a.context_kv_lens, B, t, lane);
+        b = ts.b;
+        ctx = ts.ctx;
+        i_in_seq = t - ts.first;
+        bad_len = !(ts.first <= t && t < ts.next);
     } else {
         b = (int)t;
         i_in_seq = 0;
+        ctx = ld_nc_s32(a.context_kv_lens + b);
     }
-    const int64_t ctx = ld_nc_s32(a.context_kv_lens + b);
     const int64_t pos = ctx + i_in_seq;
     const int64_t lb = pos / bs;
     if (bad_len || ctx < 0) {

@@ -243,19 +243,19 @@ __device__ __forceinline__ void append_row(const GatherArgs &a, const AppendArgs
 
     // slot of token t (warp-uniform)
     int b;
-    int64_t i_in_seq;
+    int64_t i_in_seq, ctx;
     bool bad_len = false;
     if (p.cu_q_lens != nullptr) {
-        b = seq_of_token(p.cu_q_lens, B, t, lane);
-        const int64_t first = ld_nc_s32(p.cu_q_lens + b);
-        const int64_t next = ld_nc_s32(p.cu_q_lens + b + 1);
-        i_in_seq = t - first;
-        bad_len = !(first <= t && t < next);
+        const TokenSeq ts = seq_ctx_of_token(p.cu_q_lens, p.context_kv_lens, B, t, lane);
+        b = ts.b;
+        ctx = ts.ctx;
+        i_in_seq = t - ts.first;
+        bad_len = !(ts.first <= t && t < ts.next);
     } else {
         b = (int)t;
         i_in_seq = 0;
+        ctx = ld_nc_s32(p.context_kv_lens + b);
     }
-    const int64_t ctx = ld_nc_s32(p.context_kv_lens + b);
     const int64_t pos = ctx + i_in_seq;
     // pos < 2^32: a 32-bit division (ctx and the token index are below 2^31)
     const int64_t lb = pos >= 0 ? (int64_t)((uint32_t)pos / (uint32_t)bs) : -1;

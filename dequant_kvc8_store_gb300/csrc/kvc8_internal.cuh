@@ -72,14 +72,21 @@ __device__ __forceinline__ void report(int32_t *dev_error, int32_t code) {
     if (dev_error != nullptr) atomicCAS(dev_error, 0, code);
 }
 
-// Sequence of a new token (shared by the int8 and bf16 stores).
-// Largest b in [0, B] with cu[b] <= t (cu[0] = 0 <= t < cu[B]), found by the
-// whole warp: each round samples 32 evenly spaced entries of the current range
-// at once and keeps the last sample <= t, so the range shrinks 32-fold per
-// round (two rounds for a thousand sequences).  All lanes get the same answer.
-__device__ __forceinline__ int seq_of_token(const int32_t *cu, int B, int64_t t, int lane) {
+// Sequence b of new token t with cu[b], cu[b+1] and ctx[b], in as few
+// dependent loads as the search allows: coarse ballot rounds narrow [lo, hi)
+// to at most 32 sequences, then lane j loads cu[lo+j], cu[lo+j+1] and
+// ctx[lo+j] at once and the answer's three values come back by shuffles.
+// All lanes get the same result; if t lies past cu[hi], b = hi - 1 and
+// [first, next) does not contain t (the caller reports it).
+struct TokenSeq {
+    int b;
+    int64_t first, next, ctx;
+};
+
+__device__ __forceinline__ TokenSeq seq_ctx_of_token(const int32_t *cu, const int32_t *ctx, int B,
+                                                     int64_t t, int lane) {
     int lo = 0, hi = B;  // cu[lo] <= t < cu[hi]
-    while (hi - lo > 1) {
+    while (hi - lo > 32) {
         const int step = (hi - lo + 31) >> 5;
         const int idx = lo + step * (lane + 1);
         const bool le = idx < hi && (int64_t)ld_nc_s32(cu + idx) <= t;
@@ -87,7 +94,21 @@ __device__ __forceinline__ int seq_of_token(const int32_t *cu, int B, int64_t t,
         if (m != 0u) lo += step * (32 - __clz(m));
         hi = min(hi, lo + step);
     }
-    return lo;
+    const int j = lo + lane;
+    int32_t c0 = 0, c1 = 0x7FFFFFFF, cx = 0;
+    if (j < hi) {
+        c0 = ld_nc_s32(cu + j);
+        c1 = ld_nc_s32(cu + j + 1);
+        cx = ld_nc_s32(ctx + j);
+    }
+    const unsigned m = __ballot_sync(0xFFFFFFFFu, j < hi && (int64_t)c1 <= t);
+    const int k = min(__popc(m), hi - lo - 1);
+    TokenSeq r;
+    r.b = lo + k;
+    r.first = __shfl_sync(0xFFFFFFFFu, c0, k);
+    r.next = __shfl_sync(0xFFFFFFFFu, c1, k);
+    r.ctx = __shfl_sync(0xFFFFFFFFu, cx, k);
+    return r;
 }
 
 // ---------------------------------------------------------------------------

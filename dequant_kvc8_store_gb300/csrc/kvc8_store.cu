@@ -212,19 +212,19 @@ store_kernel(const StoreArgs a) {
             }
             // ---- slot of token t (warp-uniform), overlapping the loads ----
             int b;
-            int64_t i_in_seq;
+            int64_t i_in_seq, ctx;
             bool bad_len = false;
             if (a.cu_q_lens != nullptr) {
-                b = seq_of_token(a.cu_q_lens, B, t, lane);
-                const int64_t first = ld_nc_s32(a.cu_q_lens + b);
-                const int64_t next = ld_nc_s32(a.cu_q_lens + b + 1);
-                i_in_seq = t - first;
-                bad_len = !(first <= t && t < next);
+                const TokenSeq ts = seq_ctx_of_token(a.cu_q_lens, a.context_kv_lens, B, t, lane);
+                b = ts.b;
+                ctx = ts.ctx;
+                i_in_seq = t - ts.first;
+                bad_len = !(ts.first <= t && t < ts.next);
             } else {
                 b = (int)t;
                 i_in_seq = 0;
+                ctx = ld_nc_s32(a.context_kv_lens + b);
             }
-            const int64_t ctx = ld_nc_s32(a.context_kv_lens + b);
             const int64_t pos = ctx + i_in_seq;
             // pos < 2^32 always (ctx and the token index are below 2^31):
             // floor(pos / bs) is the high word of pos * ceil(2^64 / bs)
