@@ -166,7 +166,7 @@ __device__ __forceinline__ void pv_tile(const float *s_tab_v, const Tile<D> &t, 
     for (int i = 0; i < KS; ++i) {
         float sd0 = 0.0f, sd1 = 0.0f;
         if (MODE == 1) {
-            const float2 t2 = *reinterpret_cast<const float2 *>(s_tab_v + gid * VB + 2 * i);
+            const float2 t2 = *reinterpret_cast<const float2 *>(s_tab_v + gid * (VB + 2) + 2 * i);
             sd0 = t2.x;
             sd1 = t2.y;
         }
@@ -197,7 +197,8 @@ __device__ __forceinline__ void compute_tile(const AttnArgs &a, int h, const flo
     for (int kk = 0; kk < KS; ++kk) {
         float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
         if (MODE == 1) {
-            const float4 t4 = *reinterpret_cast<const float4 *>(s_tab + h * D + tig * KB + 4 * kk);
+            const float4 t4 =
+                *reinterpret_cast<const float4 *>(s_tab + h * (D + 16) + tig * (KB + 4) + 4 * kk);
             s4[0] = t4.x; s4[1] = t4.y; s4[2] = t4.z; s4[3] = t4.w;
         }
         const float2 a01 = dequant2(t.k0[kk], 0, 1, MODE == 1 ? s4[0] : t.sk0, MODE == 1 ? s4[1] : t.sk0);
@@ -234,7 +235,7 @@ __device__ __forceinline__ void compute_tile(const AttnArgs &a, int h, const flo
         o[i][1] *= corr1; o[i][3] *= corr1;
     }
     const uint32_t pb0 = transpose8x8(plo), pb1 = transpose8x8(phi);
-    const float *s_tab_v = s_tab + (H + h) * D;
+    const float *s_tab_v = s_tab + (H + h) * (D + 16);
     if (t.valid == kSub) pv_tile<MODE, D, false>(s_tab_v, t, gid, tig, pb0, pb1, o);
     else pv_tile<MODE, D, true>(s_tab_v, t, gid, tig, pb0, pb1, o);
 }
@@ -253,15 +254,23 @@ attention_kernel(const AttnArgs a) {
     const int gid = lane >> 2, tig = lane & 3;
 
     extern __shared__ float smem[];
-    float *s_tab = smem;                                   // mode 1: [2][H][D]
-    float *s_o = smem + (MODE == 1 ? 2 * H * D : 0);       // [warps][8][D]
+    // Mode 1: the static scales [2][H][D], each row cut into the pieces one
+    // thread reads (K: four of D/4, V: eight of D/8) and each piece padded so
+    // that the pieces of a warp's threads fall in different banks.
+    float *s_tab = smem;
+    float *s_o = smem + (MODE == 1 ? 2 * H * (D + 16) : 0);  // [warps][8][D]
     float *s_m = s_o + kAttnWarps * kMaxGroup * D;         // [warps][8]
     float *s_l = s_m + kAttnWarps * kMaxGroup;             // [warps][8]
     __shared__ long long s_item;
 
     if (MODE == 1) {
-        for (int i = threadIdx.x; i < 2 * H * D; i += blockDim.x)
-            s_tab[i] = i < H * D ? ld_nc_f32(a.k_scale + i) : ld_nc_f32(a.v_scale + (i - H * D));
+        for (int i = threadIdx.x; i < 2 * H * D; i += blockDim.x) {
+            const int row = i / D, d = i - row * D;
+            if (row < H)
+                s_tab[row * (D + 16) + (d / KB) * (KB + 4) + d % KB] = ld_nc_f32(a.k_scale + i);
+            else
+                s_tab[row * (D + 16) + (d / VB) * (VB + 2) + d % VB] = ld_nc_f32(a.v_scale + (i - H * D));
+        }
         __syncthreads();
     }
     pdl_launch_dependents();  // the merge grid may launch; it waits for this one
@@ -444,7 +453,7 @@ size_t part_elems(const kvc8_geom &g) {
 template <int MODE, int D>
 cudaError_t launch_attention_variant(const AttnArgs &a, cudaStream_t stream) {
     auto kern = attention_kernel<MODE, D>;
-    const size_t smem = sizeof(float) * ((MODE == 1 ? 2 * a.g.kv_heads * D : 0) +
+    const size_t smem = sizeof(float) * ((MODE == 1 ? 2 * a.g.kv_heads * (D + 16) : 0) +
                                          kAttnWarps * kMaxGroup * (D + 2));
     static int cached_dev = -1;
     static size_t cached_smem = 0;
