@@ -83,8 +83,17 @@ struct TokenSeq {
     int64_t first, next, ctx;
 };
 
-__device__ __forceinline__ TokenSeq seq_ctx_of_token(const int32_t *cu, const int32_t *ctx, int B,
-                                                     int64_t t, int lane) {
+// The search in two halves, so that a caller can issue the loads of one token
+// and consume them later: seq_probe_begin runs the coarse rounds and issues the
+// final round's loads, seq_probe_end consumes them.
+struct SeqProbe {
+    int lo, hi;
+    int32_t c0, c1, cx;  // this lane's cu[lo+lane], cu[lo+lane+1], ctx[lo+lane]
+};
+
+__device__ __forceinline__ SeqProbe seq_probe_begin(const int32_t *cu, const int32_t *ctx, int B,
+                                                    int64_t t, int lane) {
+    SeqProbe p;
     int lo = 0, hi = B;  // cu[lo] <= t < cu[hi]
     while (hi - lo > 32) {
         const int step = (hi - lo + 31) >> 5;
@@ -94,21 +103,35 @@ __device__ __forceinline__ TokenSeq seq_ctx_of_token(const int32_t *cu, const in
         if (m != 0u) lo += step * (32 - __clz(m));
         hi = min(hi, lo + step);
     }
+    p.lo = lo;
+    p.hi = hi;
+    p.c0 = 0;
+    p.c1 = 0x7FFFFFFF;
+    p.cx = 0;
     const int j = lo + lane;
-    int32_t c0 = 0, c1 = 0x7FFFFFFF, cx = 0;
     if (j < hi) {
-        c0 = ld_nc_s32(cu + j);
-        c1 = ld_nc_s32(cu + j + 1);
-        cx = ld_nc_s32(ctx + j);
+        p.c0 = ld_nc_s32(cu + j);
+        p.c1 = ld_nc_s32(cu + j + 1);
+        p.cx = ld_nc_s32(ctx + j);
     }
-    const unsigned m = __ballot_sync(0xFFFFFFFFu, j < hi && (int64_t)c1 <= t);
-    const int k = min(__popc(m), hi - lo - 1);
+    return p;
+}
+
+__device__ __forceinline__ TokenSeq seq_probe_end(const SeqProbe &p, int64_t t, int lane) {
+    const int j = p.lo + lane;
+    const unsigned m = __ballot_sync(0xFFFFFFFFu, j < p.hi && (int64_t)p.c1 <= t);
+    const int k = min(__popc(m), p.hi - p.lo - 1);
     TokenSeq r;
-    r.b = lo + k;
-    r.first = __shfl_sync(0xFFFFFFFFu, c0, k);
-    r.next = __shfl_sync(0xFFFFFFFFu, c1, k);
-    r.ctx = __shfl_sync(0xFFFFFFFFu, cx, k);
+    r.b = p.lo + k;
+    r.first = __shfl_sync(0xFFFFFFFFu, p.c0, k);
+    r.next = __shfl_sync(0xFFFFFFFFu, p.c1, k);
+    r.ctx = __shfl_sync(0xFFFFFFFFu, p.cx, k);
     return r;
+}
+
+__device__ __forceinline__ TokenSeq seq_ctx_of_token(const int32_t *cu, const int32_t *ctx, int B,
+                                                     int64_t t, int lane) {
+    return seq_probe_end(seq_probe_begin(cu, ctx, B, t, lane), t, lane);
 }
 
 // ---------------------------------------------------------------------------
