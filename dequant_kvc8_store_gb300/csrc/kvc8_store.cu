@@ -317,7 +317,7 @@ store_kernel(const StoreArgs a) {
 #pragma unroll
                 for (int i = 0; i < W; i += 2) {
                     uint32_t mbits[4];
-                    uint32_t differ = 0u;
+                    float2 dacc = make_float2(0.0f, 0.0f);
                     float dm = 0.0f;
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
@@ -327,8 +327,11 @@ store_kernel(const StoreArgs a) {
                         if (MODE == 0) {
                             m2 = __ffma2_rn(x2, rlo2, magic2);
                             const float2 h2 = __ffma2_rn(x2, rhi2, magic2);
-                            differ |= (__float_as_uint(m2.x) ^ __float_as_uint(h2.x)) |
-                                      (__float_as_uint(m2.y) ^ __float_as_uint(h2.y));
+                            // the two ends differ by a small integer or not at all;
+                            // their squared differences add up exactly, on the
+                            // FMA pipe rather than the busier ALU pipe
+                            const float2 dd = __fadd2_rn(h2, make_float2(-m2.x, -m2.y));
+                            dacc = __ffma2_rn(dd, dd, dacc);
                         } else {
                             const float2 r2 = MODE == 2 ? make_float2(r_row, r_row)
                                               : on ? *reinterpret_cast<const float2 *>(rt + 2 * (i + e))
@@ -344,7 +347,7 @@ store_kernel(const StoreArgs a) {
                         mbits[2 * e + 1] = __float_as_uint(m2.y);
                     }
                     cw[i / 2] = pack_lo_bytes(mbits[0], mbits[1], mbits[2], mbits[3]);
-                    const bool near = (MODE == 0) ? (differ != 0u) : (dm >= kNearTie);
+                    const bool near = (MODE == 0) ? (dacc.x + dacc.y != 0.0f) : (dm >= kNearTie);
                     fix |= near ? (1u << (i / 2)) : 0u;
                 }
                 if (force_exact) fix = (1u << (W / 2)) - 1u;
