@@ -240,9 +240,10 @@ __device__ __forceinline__ void compute_tile(const AttnArgs &a, int h, const flo
     else pv_tile<MODE, D, true>(s_tab_v, t, gid, tig, pb0, pb1, o);
 }
 
-// One work item = (split j of sequence b, kv head h).
+// One work item = (split j of sequence b, kv head h).  Mode 1 is held to four
+// CTAs per SM (its scale-table reads otherwise push it past 128 registers).
 template <int MODE, int D>
-__global__ void __launch_bounds__(kAttnThreads)
+__global__ void __launch_bounds__(kAttnThreads, MODE == 1 ? 4 : 0)
 attention_kernel(const AttnArgs a) {
     constexpr int KB = D / 4;   // K code bytes per thread per position
     constexpr int VB = D / 8;   // V code bytes per thread per position
