@@ -7,6 +7,7 @@ and round-to-nearest-even conversions being exact.
 """
 from __future__ import annotations
 
+import fcntl
 import os
 import shutil
 import subprocess
@@ -49,6 +50,16 @@ def build(force: bool = False, verbose: bool = False, csrc: str = CSRC, out_dir:
     if not force and csrc == CSRC and not _stale():
         return LIB_PATH
     os.makedirs(out_dir, exist_ok=True)
+    # one build at a time per output folder (parallel test workers may all
+    # find the library stale); the first one builds, the others reuse it
+    with open(os.path.join(out_dir, ".lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        if not force and csrc == CSRC and not _stale():
+            return LIB_PATH
+        return _build_locked(csrc, out_dir, lib_path, verbose)
+
+
+def _build_locked(csrc: str, out_dir: str, lib_path: str, verbose: bool) -> str:
     cc = nvcc()
 
     def compile_one(src):

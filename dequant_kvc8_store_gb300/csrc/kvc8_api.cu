@@ -25,6 +25,10 @@ namespace {
 
 constexpr int kMaxHeadDim = 256;
 constexpr int64_t kMaxStaticTable = 12288;  // kv_heads * head_dim, mode-1 store shared memory
+// Appended rows (tokens x 2 x kv_heads) up to which the fused append + gather
+// beats the store followed by a gather (measured on decode-shaped batches:
+// 16 384 rows still won, 65 536 lost).
+constexpr int64_t kFusedAppendMaxRows = 16384;
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -127,9 +131,12 @@ kvc8_status kvc8_store(const kvc8_geom *g, int64_t num_tokens, const void *key_s
     return cuda_status(launch_store(a, stream));
 }
 
+// The plan, then room for one int32 per sequence (the spans of a long
+// append, which kvc8_append_gather gathers in a second pass).
 size_t kvc8_gather_workspace_bytes(const kvc8_geom *g) {
     if (g == nullptr || g->num_seqs < 0) return 0;
-    return plan_bytes(g->num_seqs);
+    return plan_bytes(g->num_seqs) +
+           align_up(sizeof(int32_t) * (size_t)(g->num_seqs > 0 ? g->num_seqs : 1), kAlign);
 }
 
 kvc8_status kvc8_build_metadata(const kvc8_geom *g, const int32_t *context_lengths,
@@ -303,6 +310,39 @@ kvc8_status kvc8_append_gather(const kvc8_geom *g, int64_t num_tokens, const voi
                                  out_rows, out_tok_stride, out_head_stride, workspace,
                                  workspace_bytes, dev_error, &a, &p);
     if (st != KVC8_OK) return st;
+    // A long append (a prompt rather than a decode step) is faster as the
+    // store kernel followed by a gather of every position: the fused kernel's
+    // append rows follow the definition with one division per value.
+    const size_t span_at = plan_bytes(g->num_seqs);
+    const bool long_append =
+        num_tokens * 2 * g->kv_heads > kFusedAppendMaxRows &&
+        workspace_bytes >= span_at + sizeof(int32_t) * (size_t)g->num_seqs &&
+        !(g->quant_mode == 1 && (int64_t)g->kv_heads * g->head_dim > kMaxStaticTable);
+    if (long_append) {
+        StoreArgs s;
+        s.g = *g;
+        s.num_tokens = num_tokens;
+        s.k_states = p.k_states;
+        s.v_states = p.v_states;
+        s.x_tok_stride = x_tok_stride;
+        s.x_head_stride = x_head_stride;
+        s.k_cache = key_cache;
+        s.v_cache = value_cache;
+        s.k_scale = key_scale;
+        s.v_scale = value_scale;
+        s.block_table = block_table;
+        s.cu_q_lens = cu_q_lens;
+        s.context_kv_lens = context_kv_lens;
+        s.dev_error = dev_error;
+        s.bs_magic = g->block_size >= 2 ? ~0ull / (unsigned long long)g->block_size + 1ull : 0ull;
+        if (launch_store(s, stream) != cudaSuccess) return KVC8_ERR_CUDA;
+        int32_t *spans = reinterpret_cast<int32_t *>(static_cast<char *>(workspace) + span_at);
+        if (launch_plan_span(*g, context_kv_lens, cu_q_lens, context_seq_offset, workspace, spans,
+                             dev_error, stream) != cudaSuccess)
+            return KVC8_ERR_CUDA;
+        a.context_lengths = spans;
+        return cuda_status(launch_gather(a, /*use_pdl=*/true, stream));
+    }
     if (launch_plan_append(*g, context_kv_lens, cu_q_lens, context_seq_offset, nullptr,
                            workspace, dev_error, stream) != cudaSuccess)
         return KVC8_ERR_CUDA;

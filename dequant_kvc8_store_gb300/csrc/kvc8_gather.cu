@@ -63,10 +63,13 @@ __global__ void __launch_bounds__(kPlanThreads)
 plan_kernel(const kvc8_geom g, const int32_t *__restrict__ lens,
             const int64_t *__restrict__ given_off, int64_t *__restrict__ offsets_out,
             char *__restrict__ plan, int32_t *__restrict__ dev_error,
-            const int32_t *__restrict__ cu_q, int q_mode) {
-    // lens: the positions gathered from the cache per sequence.  q_mode 0:
-    // the output rows of a sequence are exactly those; 1: an append adds
-    // cu_q[b+1] - cu_q[b] rows after them; 2: an append adds one row.
+            const int32_t *__restrict__ cu_q, int q_mode, int32_t *__restrict__ spans_out) {
+    // lens: the positions cached per sequence.  q_mode 0: the output rows of
+    // a sequence are exactly those; 1: an append adds cu_q[b+1] - cu_q[b]
+    // rows after them (the fused append computes them, so tiles cover only
+    // lens); 2: as 1 with one row; 3 and 4: as 1 and 2 with the new tokens
+    // already in the cache, so tiles cover lens + new.  spans_out, if given,
+    // receives lens + new per sequence.
     // The gather may start launching now; it waits for this grid to finish
     // (griddepcontrol.wait) before it reads the plan.
     pdl_launch_dependents();
@@ -93,16 +96,18 @@ plan_kernel(const kvc8_geom g, const int32_t *__restrict__ lens,
                 len = 0;
             }
             int64_t q = 0;
-            if (q_mode == 1) {
+            if (q_mode == 1 || q_mode == 3) {
                 q = (int64_t)cu_q[i + 1] - cu_q[i];
                 if (q < 0) {
                     report(dev_error, KVC8_DEV_BAD_LENGTH);
                     q = 0;
                 }
-            } else if (q_mode == 2) {
+            } else if (q_mode == 2 || q_mode == 4) {
                 q = 1;
             }
             span = len + q;
+            if (spans_out != nullptr) spans_out[i] = (int32_t)min(span, (int64_t)INT32_MAX);
+            if (q_mode >= 3) len = span;  // the gather reads every position
             int64_t t64 = (len + bs - 1) / bs;
             if (t64 > MB) {
                 report(dev_error, KVC8_DEV_POS_BEYOND_TABLE);
@@ -541,7 +546,17 @@ cudaError_t launch_plan(const kvc8_geom &g, const int32_t *context_lengths,
                         int32_t *dev_error, cudaStream_t stream) {
     plan_kernel<<<1, kPlanThreads, 0, stream>>>(g, context_lengths, context_seq_offset,
                                                 offsets_out, static_cast<char *>(plan), dev_error,
-                                                nullptr, 0);
+                                                nullptr, 0, nullptr);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_plan_span(const kvc8_geom &g, const int32_t *context_kv_lens,
+                             const int32_t *cu_q_lens, const int64_t *context_seq_offset,
+                             void *plan, int32_t *spans_out, int32_t *dev_error,
+                             cudaStream_t stream) {
+    plan_kernel<<<1, kPlanThreads, 0, stream>>>(g, context_kv_lens, context_seq_offset, nullptr,
+                                                static_cast<char *>(plan), dev_error, cu_q_lens,
+                                                cu_q_lens != nullptr ? 3 : 4, spans_out);
     return cudaGetLastError();
 }
 
@@ -551,7 +566,7 @@ cudaError_t launch_plan_append(const kvc8_geom &g, const int32_t *context_kv_len
                                cudaStream_t stream) {
     plan_kernel<<<1, kPlanThreads, 0, stream>>>(g, context_kv_lens, context_seq_offset,
                                                 offsets_out, static_cast<char *>(plan), dev_error,
-                                                cu_q_lens, cu_q_lens != nullptr ? 1 : 2);
+                                                cu_q_lens, cu_q_lens != nullptr ? 1 : 2, nullptr);
     return cudaGetLastError();
 }
 

@@ -293,6 +293,13 @@ cudaError_t launch_plan_append(const kvc8_geom &g, const int32_t *context_kv_len
                                const int32_t *cu_q_lens, const int64_t *context_seq_offset,
                                int64_t *offsets_out, void *plan, int32_t *dev_error,
                                cudaStream_t stream);
+// Plan of a gather over the cached and the newly stored positions
+// (tiles and offsets over context_kv_lens + new), the spans written to
+// spans_out[B] for the gather to read as its lengths.
+cudaError_t launch_plan_span(const kvc8_geom &g, const int32_t *context_kv_lens,
+                             const int32_t *cu_q_lens, const int64_t *context_seq_offset,
+                             void *plan, int32_t *spans_out, int32_t *dev_error,
+                             cudaStream_t stream);
 // The fused append + gather launch (a programmatic dependent of the plan when use_pdl).
 cudaError_t launch_append_gather(const GatherArgs &a, const AppendArgs &p, bool use_pdl,
                                  cudaStream_t stream);

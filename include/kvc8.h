@@ -153,8 +153,9 @@ kvc8_status kvc8_store(const kvc8_geom *g, int64_t num_tokens,
                        const int32_t *context_kv_lens, int32_t *dev_error,
                        cudaStream_t stream);
 
-/* Bytes of device workspace that kvc8_build_metadata and kvc8_dequant_gather
- * need for this geometry (depends on num_seqs only).  Host function. */
+/* Bytes of device workspace that kvc8_build_metadata, kvc8_dequant_gather
+ * and kvc8_append_gather need for this geometry (depends on num_seqs only;
+ * the gathers use the first part, the plan).  Host function. */
 size_t kvc8_gather_workspace_bytes(const kvc8_geom *g);
 
 /*
@@ -255,7 +256,13 @@ kvc8_status kvc8_dequant_gather_planned(const kvc8_geom *g, const int8_t *key_ca
  * to the cache and their dequantised values straight to output rows
  * offset_b + context_kv_lens[b] + i, while the same launch gathers the cached
  * positions [0, context_kv_lens[b]) from the cache.  Enqueues a plan (into
- * `workspace`) and one fused launch that overlaps the plan's tail.
+ * `workspace`) and one fused launch that overlaps the plan's tail.  A long
+ * append (more than 16 384 new K and V rows, i.e. a prompt rather than a
+ * decode step) runs instead as the store kernel, a plan over the cached and
+ * the new positions and the gather, which is faster there; that path keeps
+ * per-sequence lengths in the workspace after the plan, so it is taken only
+ * when workspace_bytes >= kvc8_gather_workspace_bytes(g).  Same results
+ * either way.
  *
  * Arguments: the new tokens, strides, caches, scales, block table, cu_q_lens
  * and context_kv_lens as in kvc8_store (num_tokens == cu_q_lens[B]); the

@@ -162,3 +162,39 @@ def test_fused_full_size_decode():
     _assert_bits_equal(bf16_bits(d.v_out.index_select(0, rows)), want_v, "v_out")
     assert not bool((d.k_out.view(torch.int16) == -1).any())
     assert not bool((d.v_out.view(torch.int16) == -1).any())
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2])
+def test_fused_long_append_takes_store_then_gather(mode):
+    """More than 16 384 appended rows: the call runs the store kernel, a plan
+    over cached + new positions and the gather; same bits as the oracle."""
+    w = W.make_workload(f"flong{mode}", q_lens=[700, 500, 1, 0], ctx_before=[30, 0, 900, 64],
+                        kv_heads=8, head_dim=128, block_size=64, num_blocks=4 * 16 + 4,
+                        quant_mode=mode, seed=280 + mode)
+    assert w.num_tokens * 2 * w.kv_heads > 16384
+    check_fused(w)
+    lens = w.context_lengths.astype(np.int64)
+    offsets = np.concatenate([[5], 5 + np.cumsum(lens + 3)[:-1]])
+    check_fused(w, offsets=offsets, out_layout="head_major", out_pad_rows=4)
+
+
+def test_fused_long_decode_append_and_small_workspace():
+    """1100 single-token sequences (cu_q_lens NULL) take the long path; with a
+    workspace that only holds the plan the call stays on the fused kernel."""
+    rng = np.random.default_rng(290)
+    ctx = rng.integers(0, 300, size=1100)
+    w = W.make_workload("flongdec", q_lens=np.ones(1100, np.int64), ctx_before=ctx, kv_heads=8,
+                        head_dim=64, block_size=64, num_blocks=1100 * 5, quant_mode=0,
+                        seed=290, decode_null_cu=True)
+    check_fused(w)
+    d = DeviceBatch(w, fill_out=0xFFFF)
+    spans_bytes = (4 * w.num_seqs + 255) // 256 * 256
+    d.ws_bytes = kv.kvc8_gather_workspace_bytes(d.g) - spans_bytes  # the plan alone
+    d.append_gather()
+    assert d.error_code() == 0
+    want_pool = _oracle_store(w)
+    _assert_pool_equal(d.host_caches(), want_pool)
+    ko, vo = oracle.dequant_gather(w.quant_mode, *want_pool, w.block_table, w.context_lengths)
+    gk, gv = d.host_outputs()
+    _assert_bits_equal(gk, ko, "k_out")
+    _assert_bits_equal(gv, vo, "v_out")
