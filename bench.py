@@ -554,7 +554,9 @@ def result_line(args, world, w, nbytes, t, clocks, e2e, has_store):
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "peak_kind": peak_kind, "traffic": traffic,
                      "algorithmic_bytes": dom_bytes},
-        "gpu_launches": args.steps * (3 if (has_store and not fused) or attention else 2),
+        # fused: plan + fused kernel, or store + plan + gather for a long append
+        "gpu_launches": args.steps * (3 if (has_store and not fused) or attention or
+                                      (fused and w.num_tokens * 2 * w.kv_heads > 16384) else 2),
         "clocks": clocks,
         "e2e": e2e,
         "wall_s": round(t["wall_s"], 3),
