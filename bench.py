@@ -76,12 +76,34 @@ WORKLOAD_TEXT = {
 }
 
 
-def source_hash() -> str:
+# the sources each timed kernel is built from (its traffic figure stays valid
+# while they are unchanged)
+KERNEL_FILES = {
+    "store_kernel": ["kvc8_store.cu", "kvc8_internal.cuh"],
+    "gather_kernel": ["kvc8_gather.cu", "kvc8_internal.cuh"],
+    "append_gather_kernel": ["kvc8_gather.cu", "kvc8_internal.cuh"],
+    "store_bf16_kernel": ["kvc8_bf16.cu", "kvc8_internal.cuh"],
+    "gather_bf16_kernel": ["kvc8_bf16.cu", "kvc8_internal.cuh"],
+    "attention_kernel": ["kvc8_attention.cu", "kvc8_internal.cuh"],
+}
+
+
+def _hash_files(paths) -> str:
     h = hashlib.sha256()
-    for p in KERNEL_SOURCES:
+    for p in paths:
         with open(os.path.join(ROOT, p), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
+
+
+def source_hash() -> str:
+    """Hash of all kernel sources."""
+    return _hash_files(KERNEL_SOURCES)
+
+
+def kernel_hash(kernel: str) -> str:
+    """Hash of the sources one kernel is built from."""
+    return _hash_files("dequant_kvc8_store_gb300/csrc/" + f for f in KERNEL_FILES[kernel])
 
 
 def measured_peak():
@@ -94,18 +116,18 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def ncu_traffic(workload: str):
-    """Per-launch DRAM bytes of the dominant kernels from the committed ncu
-    summary, if it was taken on the current kernel sources."""
+def ncu_traffic(workload: str, kernel: str):
+    """Per-launch DRAM bytes of one kernel on one workload from the committed
+    ncu summary, or None unless it was taken on the kernel's current sources."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(path) as f:
-            d = json.load(f)
+            e = json.load(f)["workloads"][workload][kernel]
+        if kernel in KERNEL_FILES and e["source_hash"] == kernel_hash(kernel):
+            return int(e["bytes"])
     except Exception:
-        return {}
-    if d.get("source_hash") != source_hash():
-        return {}
-    return d.get("workloads", {}).get(workload, {})
+        pass
+    return None
 
 
 # ---------------------------------------------------------------------------- clocks
@@ -534,7 +556,7 @@ def result_line(args, world, w, nbytes, t, clocks, e2e, has_store):
         kname = "append_gather"
     if attention:
         kname = "attention"
-    traffic = ncu_traffic(args.workload).get(kname + "_kernel")
+    traffic = ncu_traffic(args.workload, kname + "_kernel")
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t["step_ms"], 5),

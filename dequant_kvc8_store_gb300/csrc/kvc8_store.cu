@@ -24,8 +24,10 @@
 // (|x r| <= 127.0001, so adding 1.5*2^23 rounds to an integer, ties to even,
 // and the low byte of the result is the code).  If the two agree, rne is
 // monotone, so rne(fl(x/s)) is that same integer.  If they differ (a value
-// within about 2^-21 relative of a half-integer; rare), the group of four
-// values is recomputed with __fdiv_rn + __float2int_rn.
+// within about 2^-21 relative of a half-integer, in practice almost always an
+// exact tie x/s = n + 1/2; about 2 values in 10^4 of bf16 data), the group of
+// four values is recomputed in registers by code_exact, which decides the
+// rounding from one exact remainder |x| - (n + 1/2) s instead of a division.
 //
 // Static modes (s per channel, quant_mode 1, from a shared-memory table; or s
 // per block and kv head, quant_mode 2, read once per row; y = fl(x * fl(1/s))
@@ -70,6 +72,41 @@ __device__ __forceinline__ int quant_one(float x, float s, float r) {
     float d = __fsub_rn(y, __fsub_rn(m, kMagic));
     if (fabsf(d) >= kNearTie) return quant_exact(x, s);
     return __float_as_int(m) - 0x4B400000;
+}
+
+// Lower bound on the scales for which code_exact below is exact (all of its
+// intermediate quantities stay normal).
+constexpr float kExactMinScale = 0x1p-100f;
+
+// rne(fl(x / s)) clamped to [-127, 127], for a bf16 value x, a scale
+// 2^-100 <= s <= 2^120 and r = fl(1/s), without dividing.  With t = |x|/s
+// and y = fl(|x| r) (|y - t| <= 2^-23 y), let n = floor(y) and h = n + 1/2.
+// d = |x| - h s is a multiple of 2^(e_s - 24) (e_s the exponent of s) because
+// |x| has 8 significant bits and |x| >= h s / 2; so wherever
+// |t - h| < 2^-13, |d| < 2^12 of those units and the fma computes d exactly;
+// elsewhere its sign is still exact and |d| is far above the bounds below.
+// fl(t) equals h exactly when t lies within half the spacing of floats
+// around h (closed interval: h has an even significand, so the midpoints
+// round to it), i.e. when -s u_lo <= d <= s u_hi with u_hi = ulp(h)/2 and
+// u_lo = u_hi except u_lo = u_hi/2 at h = 1/2, the one power of two among
+// the half-integers.  Then rne picks the even neighbour; otherwise fl(t) lies
+// on the same side of h as t, and the code is n or n + 1 by the sign of d.
+__device__ __forceinline__ int code_exact(float x, float s, float r) {
+    const float ax = fabsf(x);
+    const float y = __fmul_rn(ax, r);
+    int q = 127;  // y >= 127 means t >= 126.99998, which rounds to 127 or more
+    if (y < 127.0f) {
+        const float n = floorf(y);
+        const float h = __fadd_rn(n, 0.5f);
+        const float d = __fmaf_rn(-h, s, ax);
+        const float u_hi = __int_as_float((__float_as_int(h) & 0x7F800000) - (24 << 23));
+        const float u_lo = h == 0.5f ? __fmul_rn(u_hi, 0.5f) : u_hi;
+        const int ni = (int)n;
+        const bool on_h = d <= __fmul_rn(s, u_hi) && d >= -__fmul_rn(s, u_lo);
+        q = on_h ? ni + (ni & 1) : (d > 0.0f ? ni + 1 : ni);
+        q = min(q, 127);
+    }
+    return x < 0.0f ? -q : q;
 }
 
 __device__ __forceinline__ uint32_t pack_lo_bytes(uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
@@ -350,7 +387,35 @@ store_kernel(const StoreArgs a) {
                     const bool near = (MODE == 0) ? (dacc.x + dacc.y != 0.0f) : (dm >= kNearTie);
                     fix |= near ? (1u << (i / 2)) : 0u;
                 }
-                if (force_exact) fix = (1u << (W / 2)) - 1u;
+                // Dynamic mode: the flagged groups (nearly all exact ties,
+                // x/s = n + 1/2) are recomputed in registers by code_exact
+                // before the store.  The static modes keep the out-of-line
+                // pass after the store (fewer registers at four CTAs per SM).
+                bool slow = force_exact || (MODE == 0 && fix != 0u && !(s_row >= kExactMinScale));
+                if (MODE == 0 && !slow && fix != 0u) {
+                    uint32_t f = fix;
+                    do {
+                        const int q = __ffs(f) - 1;
+                        f &= f - 1u;
+                        uint32_t w0 = w[k][0], w1 = w[k][1];
+#pragma unroll
+                        for (int g = 1; g < W / 2; ++g)
+                            if (q == g) {
+                                w0 = w[k][2 * g];
+                                w1 = w[k][2 * g + 1];
+                            }
+                        const uint32_t cq = pack_lo_bytes(
+                            (uint32_t)code_exact(__uint_as_float(w0 << 16), s_row, r_row),
+                            (uint32_t)code_exact(__uint_as_float(w0 & 0xFFFF0000u), s_row, r_row),
+                            (uint32_t)code_exact(__uint_as_float(w1 << 16), s_row, r_row),
+                            (uint32_t)code_exact(__uint_as_float(w1 & 0xFFFF0000u), s_row, r_row));
+#pragma unroll
+                        for (int g = 0; g < W / 2; ++g)
+                            if (q == g) cw[g] = cq;
+                    } while (f != 0u);
+                    fix = 0u;
+                }
+                if (slow) fix = (1u << (W / 2)) - 1u;
                 if (on) {
                     int8_t *cache = kv ? a.v_cache : a.k_cache;
                     const int64_t dst_row = ((int64_t)blk * H + h) * bs + slot;
@@ -360,7 +425,7 @@ store_kernel(const StoreArgs a) {
                     if (MODE == 0 && c == 0) (kv ? a.v_scale : a.k_scale)[dst_row] = s_row;
                     if (fix != 0u) {
                         // rare: the flagged groups of four codes again, one by one,
-                        // exact where needed, over the fast codes just stored
+                        // with one division where needed, over the codes just stored
                         const uint16_t *src = (kv ? a.v_states : a.k_states) + t * a.x_tok_stride +
                                               (int64_t)h * a.x_head_stride + c * E;
                         fix_codes<MODE>(src, dst, fix, s_row, r_row, st, rt);

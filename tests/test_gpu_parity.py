@@ -207,6 +207,24 @@ def test_exact_ties_everywhere_dynamic():
     check_full(_set_states(w, gen(), gen()))
 
 
+def test_exact_ties_tiny_scales_dynamic():
+    """Exact ties on rows whose scale 2^e straddles 2^-100: above it the
+    flagged groups are recomputed in registers from one exact remainder, below
+    it they take the division; amax down to 2^-106 keeps every value normal."""
+    rng = np.random.default_rng(82)
+    w = W.make_workload("ties_tiny", q_lens=[48, 17], ctx_before=[3, 0], kv_heads=4, head_dim=128,
+                        block_size=16, num_blocks=16, quant_mode=0, seed=82)
+    N, H, D = w.num_tokens, w.kv_heads, w.head_dim
+    def gen():
+        e = rng.integers(-113, -90, size=(N, H, 1)).astype(np.float32)
+        j = rng.integers(-127, 127, size=(N, H, D)).astype(np.float32)
+        x = (j + 0.5) * np.exp2(e)
+        x[:, :, 0] = 127 * np.exp2(e[:, :, 0])
+        x[:, :, 1::2] = np.round(x[:, :, 1::2] / np.exp2(e)) * np.exp2(e)  # half the values off the ties
+        return _f32_to_bits(x)
+    check_full(_set_states(w, gen(), gen()))
+
+
 def test_reciprocal_traps_and_special_rows_dynamic():
     """Rows whose entries sit at amax/2 (quotients within 2e-6 of 63.5, where
     x * (1/s) and x / s round differently), all-zero rows, and rows of bf16
