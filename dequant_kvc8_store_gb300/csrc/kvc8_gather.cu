@@ -367,7 +367,17 @@ gather_kernel(const GatherArgs a, const AppendArgs p) {
     const char *plan = static_cast<const char *>(a.plan);
     const PlanHeader *hdr = reinterpret_cast<const PlanHeader *>(plan);
     const int64_t *off = reinterpret_cast<const int64_t *>(plan + plan_offsets_at(B));
-    const int32_t *ts = reinterpret_cast<const int32_t *>(plan + plan_tile_start_at(B));
+    const int32_t *ts_g = reinterpret_cast<const int32_t *>(plan + plan_tile_start_at(B));
+    // tile_start in shared memory when it fits: each item's sequence is then
+    // found without a chain of dependent global loads
+    constexpr int kTsShared = 1024;
+    __shared__ int32_t s_ts[kTsShared];
+    const int32_t *ts = ts_g;
+    if (B + 1 <= kTsShared) {
+        for (int i = threadIdx.x; i <= B; i += blockDim.x) s_ts[i] = ts_g[i];
+        __syncthreads();
+        ts = s_ts;
+    }
     unsigned long long *counter =
         reinterpret_cast<unsigned long long *>(const_cast<int64_t *>(&hdr->work_counter));
     const int64_t items = hdr->total_tiles * H + (APPEND ? p.items : 0);

@@ -119,12 +119,28 @@ SMALL = [
          block_size=16, num_blocks=64, quant_mode=2, decode_null_cu=True),
     dict(q_lens=[77, 3, 140], ctx_before=[5, 0, 60], kv_heads=16, head_dim=128,
          block_size=32, num_blocks=30, quant_mode=2, block_scale_range=(0.002, 0.5)),
+    # odd block size: the small dynamic-scale gather keeps whole tiles
+    dict(q_lens=[20, 1, 9], ctx_before=[6, 13, 0], kv_heads=4, head_dim=64, block_size=7,
+         num_blocks=24, quant_mode=0),
 ]
 
 
 @pytest.mark.parametrize("i", range(len(SMALL)))
 def test_small_ragged(i):
     w = W.make_workload(f"small{i}", seed=50 + i, **SMALL[i])
+    check_full(w)
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_many_sequences(mode):
+    """1 500 sequences: more than the gather keeps of the tile table in shared
+    memory (it searches the plan in global memory)."""
+    rng = np.random.default_rng(90 + mode)
+    B = 1500
+    ctx = rng.integers(0, 40, size=B)
+    q = rng.integers(0, 3, size=B)
+    w = W.make_workload(f"many{mode}", q_lens=q, ctx_before=ctx, kv_heads=2, head_dim=64,
+                        block_size=16, num_blocks=B * 3 + 8, quant_mode=mode, seed=90 + mode)
     check_full(w)
 
 
