@@ -73,6 +73,9 @@ WORKLOAD_TEXT = {
                      "one static scale per (block, kv head) U[0.01,0.1]",
     "decode_small": "decode batch cut to 64 sequences (profiling size): 1 new token, cached "
                     "U[1,8192], 8 x 128, block 128, 4160-block pool, dynamic scales",
+    "mixed_small": "chunked-prefill mix with short contexts (profiling size): 64 seqs (32 "
+                   "decode, 32 chunks U[256,2048]), cached U[0,1024], 8 x 128, block 64, "
+                   "3328-block pool, static scales U[0.005,0.05]",
 }
 
 

@@ -300,8 +300,23 @@ def decode_small(seed: int = 1006) -> Workload:
                          max_blocks_per_seq=65, quant_mode=0, seed=seed)
 
 
+def mixed_small(seed: int = 1007) -> Workload:
+    """The chunked-prefill mix with cached contexts cut to U[0, 1024] and a
+    pool to match (about 1 GB on the device): the size for detailed profiles
+    of the static-scale store."""
+    rng = np.random.default_rng([seed, 99])
+    is_chunk = np.zeros(64, bool)
+    is_chunk[rng.permutation(64)[:32]] = True
+    q = np.where(is_chunk, rng.integers(256, 2048, size=64, endpoint=True), 1)
+    ctx = rng.integers(0, 1024, size=64, endpoint=True)
+    return make_workload("mixed_small", q_lens=q, ctx_before=ctx, kv_heads=8, head_dim=128,
+                         block_size=64, num_blocks=64 * 52, max_blocks_per_seq=52,
+                         quant_mode=1, seed=seed)
+
+
 NAMED = {"tiny": tiny, "prefill": prefill, "decode": decode, "mixed": mixed,
-         "longctx": longctx, "prefill_block": prefill_block, "decode_small": decode_small}
+         "longctx": longctx, "prefill_block": prefill_block, "decode_small": decode_small,
+         "mixed_small": mixed_small}
 
 
 def algorithmic_bytes(w: Workload) -> dict:
