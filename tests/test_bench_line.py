@@ -35,3 +35,37 @@ def test_result_line_for_every_path(path, gather_only):
         assert line["gpu_launches"] == 7 * (2 if one_op or gather_only else 3)
     if path == "fused":
         assert line["ops"]["store"]["ms"] == 0.0
+
+
+def test_traffic_entries_follow_their_kernel_sources(tmp_path, monkeypatch):
+    """A committed traffic figure is used only while its own kernel's sources
+    hash as they did at capture; editing one kernel leaves the others valid."""
+    root = tmp_path
+    csrc = root / "dequant_kvc8_store_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    for f in ("kvc8_store.cu", "kvc8_gather.cu", "kvc8_internal.cuh"):
+        (csrc / f).write_text(f"// {f}\n")
+    monkeypatch.setattr(bench, "ROOT", str(root))
+    (root / "profiles").mkdir()
+    entries = {"store_kernel": {"bytes": 11, "source_hash": bench.kernel_hash("store_kernel")},
+               "gather_kernel": {"bytes": 22, "source_hash": bench.kernel_hash("gather_kernel")}}
+    (root / "profiles" / "ncu_traffic.json").write_text(
+        json.dumps({"workloads": {"prefill": entries}}))
+    assert bench.ncu_traffic("prefill", "store_kernel") == 11
+    assert bench.ncu_traffic("prefill", "gather_kernel") == 22
+    assert bench.ncu_traffic("decode", "gather_kernel") is None
+    (csrc / "kvc8_store.cu").write_text("// changed\n")
+    assert bench.ncu_traffic("prefill", "store_kernel") is None
+    assert bench.ncu_traffic("prefill", "gather_kernel") == 22
+    (csrc / "kvc8_internal.cuh").write_text("// shared header changed\n")
+    assert bench.ncu_traffic("prefill", "gather_kernel") is None
+
+
+def test_committed_traffic_file_is_well_formed():
+    with open(bench.os.path.join(bench.ROOT, "profiles", "ncu_traffic.json")) as f:
+        d = json.load(f)
+    for wl, ks in d["workloads"].items():
+        assert wl in W.NAMED
+        for k, e in ks.items():
+            assert k in bench.KERNEL_FILES
+            assert int(e["bytes"]) > 0 and len(e["source_hash"]) == 16
