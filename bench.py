@@ -22,7 +22,8 @@ Printed: one JSON line (rank 0).  value = algorithmic HBM bytes of store +
 gather per step / step time, in GB/s; tokens/s and GB/s of each op are in
 "ops".  e2e = the same metric through the public API with the new tokens and
 metadata copied host->device and the gathered K/V copied device->host (pinned
-buffers) inside the timed region.  --impl reference times the CPU oracle
+buffers) inside the timed region; consecutive steps overlap their uploads,
+kernels and downloads on three streams, as a serving loop would.  --impl reference times the CPU oracle
 instead (the reference arm: a plain single-threaded restatement of the method).
 """
 from __future__ import annotations
@@ -302,18 +303,31 @@ def run_gpu(args, rank, world):
              "gather_ms": float(np.mean(ga_ms)), "wall_s": wall}
     local["step_ms"], local["store_ms"], local["gather_ms"] = reduce_max(
         [local["step_ms"], local["store_ms"], local["gather_ms"]], device=dev)
-    e2e = run_e2e(args, w, d, dev, nbytes, attn) if rank == 0 else None
+    def make_twin():
+        # a second device copy of the batch for the overlapped end-to-end loop
+        if args.path == "bf16":
+            d2 = Bf16Batch(w, device=dev, seed=rank_seed(args.workload, rank))
+        else:
+            d2 = DeviceBatch(w, device=dev)
+        a2 = (DecodeAttention(d2, ATTN_GROUP, seed=rank_seed(args.workload, rank))
+              if attn is not None else None)
+        return d2, a2
+    e2e = run_e2e(args, w, d, dev, nbytes, attn, make_twin) if rank == 0 else None
     return w, nbytes, local, clocks.summary(), e2e, has_store
 
 
-def run_e2e(args, w, d, dev, nbytes, attn=None):
+def run_e2e(args, w, d, dev, nbytes, attn, make_twin):
     """Same step through the public API with host buffers: H2D of the new K/V
     and the batch metadata from pinned memory, store, plan, gather, D2H of the
-    gathered K/V into pinned memory -- all inside the timed region."""
+    gathered K/V into pinned memory -- all of every step inside the timed
+    region.  As a serving loop would, consecutive steps overlap on three
+    streams: step i+1's inputs go up while step i computes and step i-1's
+    results come down (two device buffer sets, used alternately)."""
     import torch
     from dequant_kvc8_store_gb300.device import _bf16
 
-    stream = torch.cuda.current_stream()
+    comp = torch.cuda.current_stream()
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
     host = {}
     if d.k_states is not None:
         host["k_states"] = _bf16(w.k_states).pin_memory()
@@ -323,52 +337,87 @@ def run_e2e(args, w, d, dev, nbytes, attn=None):
         host["cu_q_lens"] = torch.from_numpy(w.cu_q_lens).pin_memory()
     host["context_kv_lens"] = torch.from_numpy(w.context_kv_lens).pin_memory()
     host["context_lengths"] = torch.from_numpy(w.context_lengths).pin_memory()
+    pair = [(d, attn), make_twin()]
     if attn is not None:  # the decode step: queries and metadata in, attention out
         host = {"block_table": host["block_table"],
                 "context_lengths": host["context_lengths"]}
         q_host = _bf16(attn.q_bits).pin_memory()
-        out_k = torch.empty(attn.out.shape, dtype=torch.bfloat16).pin_memory()
-        out_v = None
+        outs = [(torch.empty(attn.out.shape, dtype=torch.bfloat16).pin_memory(), None)
+                for _ in range(2)]
         h2d = sum(t.numel() * t.element_size() for t in host.values()) + q_host.numel() * 2
-        d2h = out_k.numel() * 2
+        d2h = outs[0][0].numel() * 2
     else:
-        out_k = torch.empty(d.k_out.shape, dtype=torch.bfloat16).pin_memory()
-        out_v = torch.empty(d.v_out.shape, dtype=torch.bfloat16).pin_memory()
+        outs = [(torch.empty(d.k_out.shape, dtype=torch.bfloat16).pin_memory(),
+                 torch.empty(d.v_out.shape, dtype=torch.bfloat16).pin_memory()) for _ in range(2)]
         h2d = sum(t.numel() * t.element_size() for t in host.values())
-        d2h = out_k.numel() * 2 * 2
+        d2h = outs[0][0].numel() * 2 * 2
     # bounded: at most ~16 GB of host<->device traffic, at least 3 steps
     steps = max(3, min(args.steps, 50, int(16e9 // max(1, h2d + d2h))))
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_comp = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
 
-    def step():
-        for name, t in host.items():
-            getattr(d, name).copy_(t, non_blocking=True)
-        if attn is not None:
-            attn.query.copy_(q_host, non_blocking=True)
-            attn(stream)
-            out_k.copy_(attn.out, non_blocking=True)
-            return
-        if args.path == "fused":
-            d.append_gather(stream)
+    def step(i):
+        j = i & 1
+        dj, aj = pair[j]
+        ok, ov = outs[j]
+        if i >= 2:
+            s_in.wait_event(ev_comp[j])  # step i-2 has consumed this buffer's inputs
+        with torch.cuda.stream(s_in):
+            for name, t in host.items():
+                getattr(dj, name).copy_(t, non_blocking=True)
+            if aj is not None:
+                aj.query.copy_(q_host, non_blocking=True)
+            ev_in[j].record(s_in)
+        comp.wait_event(ev_in[j])
+        if i >= 2:
+            comp.wait_event(ev_out[j])  # step i-2's results are down
+        if aj is not None:
+            aj(comp)
+        elif args.path == "fused":
+            dj.append_gather(comp)
         else:
-            d.store(stream)
-            d.gather(stream)
-        out_k.copy_(d.k_out, non_blocking=True)
-        out_v.copy_(d.v_out, non_blocking=True)
+            dj.store(comp)
+            dj.gather(comp)
+        ev_comp[j].record(comp)
+        s_out.wait_event(ev_comp[j])
+        with torch.cuda.stream(s_out):
+            if aj is not None:
+                ok.copy_(aj.out, non_blocking=True)
+            else:
+                ok.copy_(dj.k_out, non_blocking=True)
+                ov.copy_(dj.v_out, non_blocking=True)
+            ev_out[j].record(s_out)
 
-    for _ in range(3):
-        step()
+    for i in range(4):
+        step(i)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(steps):
-        step()
-    e1.record(stream)
+    e0.record(comp)
+    s_in.wait_event(e0)
+    s_out.wait_event(e0)
+    for i in range(steps):
+        step(i)
+    comp.wait_event(ev_out[(steps - 1) & 1])
+    e1.record(comp)
     torch.cuda.synchronize()
+    for (dj, aj), (ok, ov) in zip(pair, outs):
+        if dj.error_code() != 0:
+            raise RuntimeError("device error during the end-to-end steps")
+        # both buffer sets ran the same step: their downloads match the device
+        # results bit for bit (a race between the streams would show here)
+        same = (torch.equal(ok.view(torch.int16), aj.out.view(torch.int16).cpu()) if aj is not None
+                else torch.equal(ok.view(torch.int16), dj.k_out.view(torch.int16).cpu()) and
+                torch.equal(ov.view(torch.int16), dj.v_out.view(torch.int16).cpu()))
+        if not same:
+            raise RuntimeError("end-to-end downloads differ from the device results")
     ms = e0.elapsed_time(e1) / steps
     total = nbytes["store"] + nbytes["gather"]
     return {"value": round(total / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-            "ms_per_step": round(ms, 4), "steps": steps}
+            "ms_per_step": round(ms, 4), "steps": steps,
+            "overlap": "step i+1 H2D, step i kernels and step i-1 D2H on three streams, "
+                       "two device buffer sets"}
 
 
 # ---------------------------------------------------------------------------- CPU arm
