@@ -18,7 +18,7 @@ import torch
 import oracle
 import dequant_kvc8_store_gb300 as kv
 from dequant_kvc8_store_gb300 import workloads as W
-from dequant_kvc8_store_gb300.device import DeviceBatch, bf16_bits
+from dequant_kvc8_store_gb300.device import DeviceBatch
 
 pytestmark = pytest.mark.gpu
 

@@ -1,7 +1,6 @@
 """Plant plausible mistakes in copies of the oracle (on the CPU) and require
 that the pins reject every copy.  Each mutation is a textual edit of the C
 source; the committed oracle is never touched."""
-import os
 
 import pytest
 
