@@ -198,3 +198,27 @@ def test_fused_long_decode_append_and_small_workspace():
     gk, gv = d.host_outputs()
     _assert_bits_equal(gk, ko, "k_out")
     _assert_bits_equal(gv, vo, "v_out")
+
+
+@pytest.mark.parametrize("make", [W.prefill, W.mixed], ids=["prefill", "mixed"])
+def test_fused_full_size_long_append(make):
+    """The prefill and mixed batches through the fused call (more than 16 384
+    appended rows: store, span plan, gather): the whole pool, sampled output
+    rows against the oracle, and every output row written."""
+    w = make()
+    assert w.num_tokens * 2 * w.kv_heads > 16384
+    d = DeviceBatch(w, fill_out=0xFFFF)
+    d.append_gather()
+    assert d.error_code() == 0
+    oracle.store(w.quant_mode, w.k_states, w.v_states, w.k_cache, w.v_cache, w.k_scale,
+                 w.v_scale, w.block_table, w.cu_q_lens, w.context_kv_lens)
+    _assert_pool_equal(d.host_caches(), (w.k_cache, w.v_cache, w.k_scale, w.v_scale))
+    seq, pos = _sample_positions(w, np.random.default_rng(9))
+    want_k, want_v = oracle.dequant_positions(w.quant_mode, w.k_cache, w.v_cache, w.k_scale,
+                                              w.v_scale, w.block_table, seq, pos)
+    offs = oracle.exclusive_cumsum(w.context_lengths)
+    rows = torch.from_numpy(offs[seq] + pos).to("cuda")
+    _assert_bits_equal(bf16_bits(d.k_out.index_select(0, rows)), want_k, "k_out")
+    _assert_bits_equal(bf16_bits(d.v_out.index_select(0, rows)), want_v, "v_out")
+    assert not bool((d.k_out.view(torch.int16) == -1).any())
+    assert not bool((d.v_out.view(torch.int16) == -1).any())
