@@ -12,7 +12,6 @@ namespace kvc8 {
 namespace {
 
 constexpr int kWarpsPerCta = 8;
-constexpr int kChunksPerLane = 8;  // 16-byte chunks a lane keeps in flight
 constexpr int kGatherThreads = 256;
 
 // Slot of new token t (warp-uniform): physical block and in-block slot, or a
@@ -56,28 +55,42 @@ __device__ __forceinline__ Slot token_slot(const StoreBf16Args &a, int64_t t, in
 }
 
 // One warp per token: the lanes move the token's 2H rows of D bf16 values in
-// 16-byte chunks (D/8 per row), requesting up to 8 chunks each before the slot
-// lookup so that the loads overlap it.
+// chunks requested before the slot lookup, so that the loads overlap it.  WIDE
+// (inputs and caches 32-byte aligned, input strides multiples of 16 values):
+// 32-byte chunks, one 256-bit load and store each, 4 in flight per lane;
+// otherwise 16-byte chunks, 8 in flight per lane.
+template <bool WIDE>
 __global__ void __launch_bounds__(kWarpsPerCta * 32)
 store_bf16_kernel(const StoreBf16Args a) {
+    constexpr int CW = WIDE ? 16 : 8;   // values per chunk
+    constexpr int K = WIDE ? 4 : 8;     // chunks in flight per lane
     const int H = a.g.kv_heads, D = a.g.head_dim, bs = a.g.block_size;
-    const int CPR = D >> 3;           // chunks per row
-    const int nch = 2 * H * CPR;      // chunks per token
+    const int CPR = D / CW;             // chunks per row
+    const int nch = 2 * H * CPR;        // chunks per token
     const int lane = threadIdx.x & 31;
     const int64_t nwarps = (int64_t)gridDim.x * kWarpsPerCta;
     for (int64_t t = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5); t < a.num_tokens;
          t += nwarps) {
         Slot sl{0, 0, 0};
-        for (int c0 = 0; c0 < nch; c0 += 32 * kChunksPerLane) {
-            uint4 v[kChunksPerLane];
+        for (int c0 = 0; c0 < nch; c0 += 32 * K) {
+            uint4 v[K][WIDE ? 2 : 1];
 #pragma unroll
-            for (int k = 0; k < kChunksPerLane; ++k) {
+            for (int k = 0; k < K; ++k) {
                 const int c = c0 + k * 32 + lane;
                 if (c < nch) {
                     const int row = c / CPR, col = c - row * CPR;
                     const int kv = row >= H, h = row - kv * H;
-                    v[k] = ld_stream_16((kv ? a.v_states : a.k_states) + t * a.x_tok_stride +
-                                        (int64_t)h * a.x_head_stride + col * 8);
+                    const uint16_t *src = (kv ? a.v_states : a.k_states) + t * a.x_tok_stride +
+                                          (int64_t)h * a.x_head_stride + col * CW;
+                    if (WIDE) {
+                        asm("ld.global.nc.L1::no_allocate.v8.u32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                            : "=r"(v[k][0].x), "=r"(v[k][0].y), "=r"(v[k][0].z), "=r"(v[k][0].w),
+                              "=r"(v[k][WIDE ? 1 : 0].x), "=r"(v[k][WIDE ? 1 : 0].y),
+                              "=r"(v[k][WIDE ? 1 : 0].z), "=r"(v[k][WIDE ? 1 : 0].w)
+                            : "l"(src));
+                    } else {
+                        v[k][0] = ld_stream_16(src);
+                    }
                 }
             }
             if (c0 == 0) {
@@ -86,16 +99,24 @@ store_bf16_kernel(const StoreBf16Args a) {
             }
             if (sl.err != 0) break;  // warp-uniform: skip the token
 #pragma unroll
-            for (int k = 0; k < kChunksPerLane; ++k) {
+            for (int k = 0; k < K; ++k) {
                 const int c = c0 + k * 32 + lane;
                 if (c < nch) {
                     const int row = c / CPR, col = c - row * CPR;
                     const int kv = row >= H, h = row - kv * H;
                     uint16_t *dst = (kv ? a.v_cache : a.k_cache) +
-                                    ((((int64_t)sl.blk * H + h) * bs + sl.slot) * D + col * 8);
-                    asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "r"(v[k].x),
-                                 "r"(v[k].y), "r"(v[k].z), "r"(v[k].w)
-                                 : "memory");
+                                    ((((int64_t)sl.blk * H + h) * bs + sl.slot) * D + col * CW);
+                    if (WIDE) {
+                        asm volatile("st.global.v8.u32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst),
+                                     "r"(v[k][0].x), "r"(v[k][0].y), "r"(v[k][0].z), "r"(v[k][0].w),
+                                     "r"(v[k][WIDE ? 1 : 0].x), "r"(v[k][WIDE ? 1 : 0].y),
+                                     "r"(v[k][WIDE ? 1 : 0].z), "r"(v[k][WIDE ? 1 : 0].w)
+                                     : "memory");
+                    } else {
+                        asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "r"(v[k][0].x),
+                                     "r"(v[k][0].y), "r"(v[k][0].z), "r"(v[k][0].w)
+                                     : "memory");
+                    }
                 }
             }
         }
@@ -112,9 +133,27 @@ __device__ __forceinline__ int seq_of_tile(const int32_t *ts, int B, int64_t til
     return lo;
 }
 
+// 32 bytes from the cache, streamed past L1: one 256-bit load when WIDE
+// (32-byte aligned), else two 128-bit loads.
+template <bool WIDE>
+__device__ __forceinline__ void load_chunk32(const uint16_t *p, uint4 &lo, uint4 &hi) {
+    if (WIDE) {
+        asm("ld.global.nc.L1::no_allocate.v8.u32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+            : "=r"(lo.x), "=r"(lo.y), "=r"(lo.z), "=r"(lo.w), "=r"(hi.x), "=r"(hi.y),
+              "=r"(hi.z), "=r"(hi.w)
+            : "l"(p));
+    } else {
+        lo = ld_stream_16(p);
+        hi = ld_stream_16(p + 8);
+    }
+}
+
 // Work item: one tile (sequence, logical block) and a pair of its (K|V, head)
 // slabs, handed out by the plan's atomic counter, as in the int8 gather.  Each
-// thread moves one 32-byte chunk (16 values) per slab per round.
+// thread moves one 32-byte chunk (16 values) per slab per round: one 256-bit
+// load and store each when the cache, the outputs and their strides are
+// 32-byte aligned (WIDE), else two 128-bit ones.
+template <bool WIDE>
 __global__ void __launch_bounds__(kGatherThreads)
 gather_bf16_kernel(const GatherBf16Args a) {
     const int H = a.g.kv_heads, D = a.g.head_dim, bs = a.g.block_size;
@@ -163,8 +202,7 @@ gather_bf16_kernel(const GatherBf16Args a) {
                     if (c < nch) {
                         const uint16_t *src = (kv ? a.v_cache : a.k_cache) +
                                               (((int64_t)blk * H + h) * bs * D + (int64_t)c * 16);
-                        lo[sl] = ld_stream_16(src);
-                        hi[sl] = ld_stream_16(src + 8);
+                        load_chunk32<WIDE>(src, lo[sl], hi[sl]);
                     }
                 }
 #pragma unroll
@@ -175,8 +213,12 @@ gather_bf16_kernel(const GatherBf16Args a) {
                         const int row = c / CPR, col = c - row * CPR;
                         uint16_t *dst = (kv ? a.v_out : a.k_out) + (row0 + row) * a.out_tok_stride +
                                         (int64_t)h * a.out_head_stride + col * 16;
-                        st_stream_16(dst, lo[sl].x, lo[sl].y, lo[sl].z, lo[sl].w);
-                        st_stream_16(dst + 8, hi[sl].x, hi[sl].y, hi[sl].z, hi[sl].w);
+                        if (WIDE) {
+                            st_stream_32(dst, lo[sl], hi[sl]);
+                        } else {
+                            st_stream_16(dst, lo[sl].x, lo[sl].y, lo[sl].z, lo[sl].w);
+                            st_stream_16(dst + 8, hi[sl].x, hi[sl].y, hi[sl].z, hi[sl].w);
+                        }
                     }
                 }
             }
@@ -192,37 +234,44 @@ gather_bf16_kernel(const GatherBf16Args a) {
 
 cudaError_t launch_store_bf16(const StoreBf16Args &a, cudaStream_t stream) {
     if (a.num_tokens <= 0) return cudaSuccess;
-    static int cached_dev = -1, cached_occ = 0;
+    auto a32 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 31) == 0; };
+    const bool wide = a32(a.k_states) && a32(a.v_states) && a32(a.k_cache) && a32(a.v_cache) &&
+                      a.x_tok_stride % 16 == 0 && a.x_head_stride % 16 == 0;
+    auto kern = wide ? store_bf16_kernel<true> : store_bf16_kernel<false>;
+    static int cached_dev[2] = {-1, -1}, cached_occ[2] = {0, 0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (cached_dev != dev) {
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&cached_occ, store_bf16_kernel,
+    if (cached_dev[wide] != dev) {
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&cached_occ[wide], kern,
                                                           kWarpsPerCta * 32, 0);
         if (e != cudaSuccess) return e;
-        if (cached_occ < 1) cached_occ = 1;
-        cached_dev = dev;
+        if (cached_occ[wide] < 1) cached_occ[wide] = 1;
+        cached_dev[wide] = dev;
     }
     const int64_t need = (a.num_tokens + kWarpsPerCta - 1) / kWarpsPerCta;
-    const int64_t cap = (int64_t)sm_count() * cached_occ;
-    store_bf16_kernel<<<(int)(need < cap ? need : cap), kWarpsPerCta * 32, 0, stream>>>(a);
+    const int64_t cap = (int64_t)sm_count() * cached_occ[wide];
+    kern<<<(int)(need < cap ? need : cap), kWarpsPerCta * 32, 0, stream>>>(a);
     return cudaGetLastError();
 }
 
 cudaError_t launch_gather_bf16(const GatherBf16Args &a, bool use_pdl, cudaStream_t stream) {
-    static int cached_dev = -1, cached_occ = 0;
+    auto a32 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 31) == 0; };
+    const bool wide = a32(a.k_cache) && a32(a.v_cache) && a32(a.k_out) && a32(a.v_out) &&
+                      a.out_tok_stride % 16 == 0 && a.out_head_stride % 16 == 0;
+    auto kern = wide ? gather_bf16_kernel<true> : gather_bf16_kernel<false>;
+    static int cached_dev[2] = {-1, -1}, cached_occ[2] = {0, 0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (cached_dev != dev) {
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&cached_occ, gather_bf16_kernel,
-                                                          kGatherThreads, 0);
+    if (cached_dev[wide] != dev) {
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&cached_occ[wide], kern, kGatherThreads, 0);
         if (e != cudaSuccess) return e;
-        if (cached_occ < 1) cached_occ = 1;
-        cached_dev = dev;
+        if (cached_occ[wide] < 1) cached_occ[wide] = 1;
+        cached_dev[wide] = dev;
     }
     const int64_t max_items = (int64_t)a.g.num_seqs * a.g.max_blocks_per_seq * a.g.kv_heads;
-    const int64_t cap = (int64_t)sm_count() * cached_occ;
+    const int64_t cap = (int64_t)sm_count() * cached_occ[wide];
     const int grid = (int)(max_items < cap ? max_items : cap);
     if (grid <= 0) return cudaSuccess;
     cudaLaunchConfig_t cfg = {};
@@ -234,7 +283,7 @@ cudaError_t launch_gather_bf16(const GatherBf16Args &a, bool use_pdl, cudaStream
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = use_pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, gather_bf16_kernel, a);
+    return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
 }  // namespace kvc8
