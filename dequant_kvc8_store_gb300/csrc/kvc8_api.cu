@@ -1,6 +1,6 @@
 // kvc8_api.cu -- the extern "C" entry points of libkvc8 (declared in kvc8.h):
-// host-side argument checks, then the launches in kvc8_store.cu and
-// kvc8_gather.cu.  Nothing here allocates device memory or synchronises,
+// host-side argument checks, then the launches in kvc8_store.cu,
+// kvc8_gather.cu, kvc8_bf16.cu and kvc8_attention.cu.  Nothing here allocates device memory or synchronises,
 // except kvc8_get_error, whose purpose is to synchronise.
 #include <cmath>
 #include <cstdint>
