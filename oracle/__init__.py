@@ -102,11 +102,6 @@ class Oracle:
                                            P, P, P, P, P, P, P, P, P,
                                            i64, i64, i64]
         lib.orc_dequant_gather.restype = i32
-        lib.orc_dequant_positions.argtypes = [i32, i32, i32, i32, i32, i32,
-                                              P, P, P, P, P, i64, P, P, P, P]
-        lib.orc_dequant_positions.restype = i32
-        lib.orc_slots.argtypes = [i32, i32, i32, P, i64, P, P, P, P]
-        lib.orc_slots.restype = None
         lib.orc_quantize_value.argtypes = [ctypes.c_uint16, ctypes.c_float]
         lib.orc_quantize_value.restype = ctypes.c_int8
         lib.orc_dequantize_value.argtypes = [ctypes.c_int8, ctypes.c_float]
@@ -220,25 +215,6 @@ class Oracle:
                "orc_dequant_gather")
         return k_out, v_out
 
-    def dequant_positions(self, quant_mode, k_cache, v_cache, k_scale, v_scale, block_table,
-                          sample_seq, sample_pos):
-        """Dequantised K and V row sets [n][H][D] (bf16 bits) of sampled positions."""
-        kc, vc = _c(k_cache, np.int8), _c(v_cache, np.int8)
-        ks, vs = _c(k_scale, np.float32), _c(v_scale, np.float32)
-        bt = _c(block_table, np.int32)
-        sq = _c(sample_seq, np.int32)
-        sp = _c(sample_pos, np.int64)
-        NB, H, bs, D = kc.shape
-        B, MB = bt.shape
-        n = sq.shape[0]
-        k_rows = np.empty((n, H, D), np.uint16)
-        v_rows = np.empty((n, H, D), np.uint16)
-        _check(self.lib.orc_dequant_positions(quant_mode, H, D, bs, NB, MB, _ptr(kc), _ptr(vc),
-                                              _ptr(ks), _ptr(vs), _ptr(bt), n, _ptr(sq),
-                                              _ptr(sp), _ptr(k_rows), _ptr(v_rows)),
-               "orc_dequant_positions")
-        return k_rows, v_rows
-
     def store_bf16(self, k_bits, v_bits, k_cache, v_cache, block_table, cu_q_lens,
                    context_kv_lens):
         """bf16 store (no quantisation) into uint16 caches [NB][H][bs][D], in place."""
@@ -296,18 +272,6 @@ class Oracle:
                "orc_paged_decode_attention")
         return out
 
-    def slots(self, block_table, block_size, num_blocks, seq, pos):
-        """Physical (block, slot) arrays for (seq, pos) pairs; -1 where out of range."""
-        bt = _c(block_table, np.int32)
-        sq = _c(seq, np.int32)
-        sp = _c(pos, np.int64)
-        n = sq.shape[0]
-        blk = np.empty(n, np.int32)
-        slot = np.empty(n, np.int32)
-        self.lib.orc_slots(block_size, num_blocks, bt.shape[1], _ptr(bt), n, _ptr(sq),
-                           _ptr(sp), _ptr(blk), _ptr(slot))
-        return blk, slot
-
 
 _lock = threading.Lock()
 _default = None
@@ -326,7 +290,6 @@ def __getattr__(name):
     # module-level shortcuts: oracle.store(...), oracle.dequant_gather(...), ...
     if name in {"quantize_value", "dequantize_value", "round_to_bf16", "row_scale",
                 "quantize_rows", "store", "exclusive_cumsum", "dequant_gather",
-                "dequant_positions", "slots", "store_bf16", "gather_bf16",
-                "paged_decode_attention"}:
+                "store_bf16", "gather_bf16", "paged_decode_attention"}:
         return getattr(default(), name)
     raise AttributeError(name)

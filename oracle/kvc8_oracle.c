@@ -310,63 +310,6 @@ int orc_dequant_gather(int quant_mode, int num_seqs, int kv_heads,
     return ORC_OK;
 }
 
-/* Dequantise the K and V row sets of n sampled logical positions, one by one,
- * for checks at sizes where the full gather would take too long on one core.
- * sample_seq[i], sample_pos[i] name the sequence and position; k_rows and
- * v_rows receive [n][H][D] bf16 bits. */
-int orc_dequant_positions(int quant_mode, int kv_heads, int head_dim,
-                          int block_size, int num_blocks, int max_blocks_per_seq,
-                          const int8_t *k_cache, const int8_t *v_cache,
-                          const float *k_scale, const float *v_scale,
-                          const int32_t *block_table, int64_t n,
-                          const int32_t *sample_seq, const int64_t *sample_pos,
-                          uint16_t *k_rows, uint16_t *v_rows)
-{
-    if (quant_mode < 0 || quant_mode > 2)
-        return ORC_ERR_ARG;
-    for (int64_t i = 0; i < n; ++i) {
-        int32_t blk, slot;
-        int rc = orc_slot(block_table, max_blocks_per_seq, block_size,
-                          num_blocks, sample_seq[i], sample_pos[i], &blk, &slot);
-        if (rc != ORC_OK)
-            return rc;
-        for (int kv = 0; kv < 2; ++kv) {
-            const int8_t *cache = kv ? v_cache : k_cache;
-            const float *scale = kv ? v_scale : k_scale;
-            uint16_t *rows = kv ? v_rows : k_rows;
-            for (int h = 0; h < kv_heads; ++h) {
-                int64_t src_row = ((int64_t)blk * kv_heads + h) * block_size + slot;
-                for (int d = 0; d < head_dim; ++d) {
-                    float s = quant_mode == 0   ? scale[src_row]
-                              : quant_mode == 1 ? scale[h * head_dim + d]
-                                                : scale[(int64_t)blk * kv_heads + h];
-                    rows[(i * kv_heads + h) * head_dim + d] =
-                        orc_dequantize_one(cache[src_row * head_dim + d], s);
-                }
-            }
-        }
-    }
-    return ORC_OK;
-}
-
-/* Physical (block, slot) for n (sequence, position) pairs; -1 where the
- * position leaves the block table or the block id leaves the pool. */
-void orc_slots(int block_size, int num_blocks, int max_blocks_per_seq,
-               const int32_t *block_table, int64_t n, const int32_t *seq,
-               const int64_t *pos, int32_t *blk_out, int32_t *slot_out)
-{
-    for (int64_t i = 0; i < n; ++i) {
-        int32_t blk = -1, slot = -1;
-        if (orc_slot(block_table, max_blocks_per_seq, block_size, num_blocks,
-                     seq[i], pos[i], &blk, &slot) != ORC_OK) {
-            blk = -1;
-            slot = -1;
-        }
-        blk_out[i] = blk;
-        slot_out[i] = slot;
-    }
-}
-
 /* Element-level entry points, so that tests can pin each step on its own. */
 int8_t orc_quantize_value(uint16_t x_bf16, float s)
 {

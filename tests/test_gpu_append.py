@@ -13,9 +13,8 @@ import torch
 import oracle
 import dequant_kvc8_store_gb300 as kv
 from dequant_kvc8_store_gb300 import workloads as W
-from dequant_kvc8_store_gb300.device import DeviceBatch, bf16_bits
-from test_gpu_parity import (SMALL, _assert_bits_equal, _assert_pool_equal, _oracle_store,
-                             _sample_positions)
+from dequant_kvc8_store_gb300.device import DeviceBatch
+from test_gpu_parity import SMALL, _assert_bits_equal, _assert_pool_equal, _oracle_store
 
 pytestmark = pytest.mark.gpu
 
@@ -140,28 +139,28 @@ def test_fused_reports_short_output_and_stores_anyway():
     _assert_pool_equal(d.host_caches(), _oracle_store(w))
 
 
-def test_fused_full_size_decode():
-    """The decode batch at full size: the whole pool, and sampled output rows."""
-    w = W.decode()
+def _check_fused_full_size(w):
+    """One fused call on a full-size batch: the whole pool, and every element
+    of the output (each sequence's cached rows and its appended rows) against
+    the oracle's store followed by its gather."""
     d = DeviceBatch(w, fill_out=0xFFFF)
     d.append_gather()
     assert d.error_code() == 0
     oracle.store(w.quant_mode, w.k_states, w.v_states, w.k_cache, w.v_cache, w.k_scale,
                  w.v_scale, w.block_table, w.cu_q_lens, w.context_kv_lens)
     _assert_pool_equal(d.host_caches(), (w.k_cache, w.v_cache, w.k_scale, w.v_scale))
-    seq, pos = _sample_positions(w, np.random.default_rng(8))
-    # every sequence's new (last) position is among the samples
-    last = w.context_lengths.astype(np.int64) - 1
-    seq = np.concatenate([seq, np.arange(w.num_seqs, dtype=np.int32)])
-    pos = np.concatenate([pos, last])
-    want_k, want_v = oracle.dequant_positions(w.quant_mode, w.k_cache, w.v_cache, w.k_scale,
-                                              w.v_scale, w.block_table, seq, pos)
-    offs = oracle.exclusive_cumsum(w.context_lengths)
-    rows = torch.from_numpy(offs[seq] + pos).to("cuda")
-    _assert_bits_equal(bf16_bits(d.k_out.index_select(0, rows)), want_k, "k_out")
-    _assert_bits_equal(bf16_bits(d.v_out.index_select(0, rows)), want_v, "v_out")
-    assert not bool((d.k_out.view(torch.int16) == -1).any())
-    assert not bool((d.v_out.view(torch.int16) == -1).any())
+    ko, vo = oracle.dequant_gather(w.quant_mode, w.k_cache, w.v_cache, w.k_scale, w.v_scale,
+                                   w.block_table, w.context_lengths)
+    gk, gv = d.host_outputs()
+    _assert_bits_equal(gk, ko, "k_out")
+    del gk, ko
+    _assert_bits_equal(gv, vo, "v_out")
+
+
+def test_fused_full_size_decode():
+    """The decode batch at full size through the fused kernel (256 appended
+    tokens, 1.13 M gathered positions)."""
+    _check_fused_full_size(W.decode())
 
 
 @pytest.mark.parametrize("mode", [0, 1, 2])
@@ -203,22 +202,7 @@ def test_fused_long_decode_append_and_small_workspace():
 @pytest.mark.parametrize("make", [W.prefill, W.mixed], ids=["prefill", "mixed"])
 def test_fused_full_size_long_append(make):
     """The prefill and mixed batches through the fused call (more than 16 384
-    appended rows: store, span plan, gather): the whole pool, sampled output
-    rows against the oracle, and every output row written."""
+    appended rows: store, span plan, gather)."""
     w = make()
     assert w.num_tokens * 2 * w.kv_heads > 16384
-    d = DeviceBatch(w, fill_out=0xFFFF)
-    d.append_gather()
-    assert d.error_code() == 0
-    oracle.store(w.quant_mode, w.k_states, w.v_states, w.k_cache, w.v_cache, w.k_scale,
-                 w.v_scale, w.block_table, w.cu_q_lens, w.context_kv_lens)
-    _assert_pool_equal(d.host_caches(), (w.k_cache, w.v_cache, w.k_scale, w.v_scale))
-    seq, pos = _sample_positions(w, np.random.default_rng(9))
-    want_k, want_v = oracle.dequant_positions(w.quant_mode, w.k_cache, w.v_cache, w.k_scale,
-                                              w.v_scale, w.block_table, seq, pos)
-    offs = oracle.exclusive_cumsum(w.context_lengths)
-    rows = torch.from_numpy(offs[seq] + pos).to("cuda")
-    _assert_bits_equal(bf16_bits(d.k_out.index_select(0, rows)), want_k, "k_out")
-    _assert_bits_equal(bf16_bits(d.v_out.index_select(0, rows)), want_v, "v_out")
-    assert not bool((d.k_out.view(torch.int16) == -1).any())
-    assert not bool((d.v_out.view(torch.int16) == -1).any())
+    _check_fused_full_size(w)
