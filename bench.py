@@ -5,12 +5,16 @@ One step = one store of a batch's new K/V tokens into the paged cache plus one
 dequant-gather of every sequence's full context (metadata plan + gather), i.e.
 the whole hot path, through the C ABI of libkvc8.
 
-Default workload: "prefill" -- batch 16, prompts U{512..4096} into an empty
-cache, 8 kv heads x head_dim 128, block 128, 1024-block pool, dynamic
-per-token scales, N(0,1) K/V with 4 outlier channels per head (x20).  Other
-workloads: --workload tiny|decode|mixed|longctx.  --path bf16 runs the same
-step on the bf16 cache without quantisation (kvc8_store_bf16 +
-kvc8_gather_bf16) instead of the int8 one.
+Default workload: "decode" -- batch 256, one new token per sequence appended
+after U{1..8192} cached tokens, 8 kv heads x head_dim 128, block 128,
+18000-block pool, dynamic per-token scales: the store of 256 tokens plus the
+gather of 1.13 M positions (7 GB of algorithmic traffic per step), the largest
+configuration that runs both ops.  Other workloads: --workload
+tiny|prefill|mixed|longctx|...  --path bf16 runs the same step on the bf16
+cache without quantisation (kvc8_store_bf16 + kvc8_gather_bf16) instead of the
+int8 one.  On one GPU the int8 path also times the prefill, decode, mixed and
+long-context batches after the headline region and reports each op of each in
+"ops"["by_workload"] (skip with --no-workload-sweep).
 
 Timing: W untimed warm-up steps, then exactly K steps.  L2 is flushed (a
 256 MiB write, then a 256 MiB read) before each timed kernel; each op is bracketed by CUDA events on
@@ -48,6 +52,10 @@ from dequant_kvc8_store_gb300 import workloads as W  # noqa: E402
 
 FALLBACK_HBM_GBS = 6800.0
 FLUSH_BYTES = 256 << 20
+DEFAULT_WORKLOAD = "decode"
+# the full-size batches whose ops the int8 path also reports, one by one
+SWEEP_WORKLOADS = ["prefill", "decode", "mixed", "longctx"]
+L2_TEXT = "flushed before each timed op (256 MiB write, then 256 MiB read)"
 METRIC = "achieved HBM GB/s (% of ~8 TB/s) and K+V tokens/s for store and dequant"
 KERNEL_SOURCES = ["dequant_kvc8_store_gb300/csrc/kvc8_store.cu",
                   "dequant_kvc8_store_gb300/csrc/kvc8_gather.cu",
@@ -120,18 +128,38 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def ncu_traffic(workload: str, kernel: str):
-    """Per-launch DRAM bytes of one kernel on one workload from the committed
-    ncu summary, or None unless it was taken on the kernel's current sources."""
+def ncu_entry(workload: str, kernel: str):
+    """The committed ncu figures of one kernel on one workload, or None unless
+    they were taken on the kernel's current sources.  An entry holds `bytes`
+    (dram__bytes_read.sum + dram__bytes_write.sum of one full launch; scaled by
+    the units processed when the capture ran on a smaller batch, named in
+    `captured_on`), and, when known, `captured_bytes` and `captured_ns`
+    (gpu__time_duration.sum) of the captured launch itself."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(path) as f:
             e = json.load(f)["workloads"][workload][kernel]
         if kernel in KERNEL_FILES and e["source_hash"] == kernel_hash(kernel):
-            return int(e["bytes"])
+            return e
     except Exception:
         pass
     return None
+
+
+def ncu_traffic(workload: str, kernel: str):
+    """Per-launch DRAM bytes of one kernel on one workload (see ncu_entry)."""
+    e = ncu_entry(workload, kernel)
+    return None if e is None else int(e["bytes"])
+
+
+def ncu_dram_frac(workload: str, kernel: str, peak: float):
+    """The captured launch's DRAM bytes / its ncu duration / peak: the DRAM
+    rate ncu saw, beside the algorithmic-byte fraction (writes still in L2 when
+    a short kernel ends count in the algorithmic figure, not in this one)."""
+    e = ncu_entry(workload, kernel)
+    if e is None or not e.get("captured_ns"):
+        return None
+    return round(int(e["captured_bytes"]) / (float(e["captured_ns"]) * 1e-9) / 1e9 / peak, 4)
 
 
 # ---------------------------------------------------------------------------- clocks
@@ -224,6 +252,81 @@ def job_throughput(bytes_per_rank_step: int, world: int, step_ms_max: float) -> 
 
 # ---------------------------------------------------------------------------- GPU arm
 
+class Timer:
+    """L2 flush, barrier and per-op CUDA-event timing of one batch's steps."""
+
+    def __init__(self, dev, world):
+        import torch
+        self.torch = torch
+        self.world = world
+        self.stream = torch.cuda.current_stream()
+        self.flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        self.clean = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        self.sink = torch.empty((), dtype=torch.float32, device=dev)
+
+    def flush_l2(self, v):
+        # write more than L2 holds, then read another buffer that size, so L2
+        # ends up holding clean lines (no write-back competes with the next op)
+        self.flush.fill_(v)
+        self.torch.sum(self.clean, dim=0, out=self.sink)
+
+    def barrier(self):
+        if self.world > 1:
+            self.torch.distributed.barrier()
+        self.torch.cuda.synchronize()
+
+    def run(self, d, attn, path, has_store, steps, warmup, clocks=None):
+        """W untimed steps, then exactly `steps` timed ones; returns the mean
+        store / gather / step milliseconds (each op between its own events on
+        the launching stream) and the wall time of the timed region."""
+        torch, stream = self.torch, self.stream
+        one_op = path in ("fused", "attention")  # no separate store op
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+
+        def step(e=None):
+            if not one_op:
+                self.flush_l2(1)
+            if e: e[0].record(stream)
+            if has_store and not one_op:
+                d.store(stream)
+            if e: e[1].record(stream)
+            self.flush_l2(2)
+            if e: e[2].record(stream)
+            if attn is not None:
+                attn(stream)  # split plan + attention kernel + merge kernel
+            elif path == "fused":
+                d.append_gather(stream)  # plan kernel + fused append/gather kernel
+            else:
+                d.gather(stream)  # plan kernel + gather kernel (programmatic dependent launch)
+            if e: e[3].record(stream)
+
+        for _ in range(warmup):
+            step()
+        if d.error_code() != 0:
+            raise RuntimeError("device error during warm-up")
+        self.barrier()
+        t0 = time.perf_counter()
+        for i in range(steps):
+            step(ev[i])
+        self.barrier()
+        wall = time.perf_counter() - t0
+        st_ms = [0.0 if one_op else e[0].elapsed_time(e[1]) for e in ev]
+        ga_ms = [e[2].elapsed_time(e[3]) for e in ev]
+        if d.error_code() != 0:
+            raise RuntimeError("device error during the timed steps")
+        return {"step_ms": float(np.mean([a + b for a, b in zip(st_ms, ga_ms)])),
+                "store_ms": float(np.mean(st_ms)), "gather_ms": float(np.mean(ga_ms)),
+                "wall_s": wall}
+
+
+def gpu_uuid(dev):
+    import torch
+    try:
+        return "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        return None
+
+
 def run_gpu(args, rank, world):
     import torch
     import dequant_kvc8_store_gb300 as kv
@@ -240,69 +343,13 @@ def run_gpu(args, rank, world):
         d = DeviceBatch(w, device=dev)
     attn = (DecodeAttention(d, ATTN_GROUP, seed=rank_seed(args.workload, rank))
             if args.path == "attention" else None)
-    stream = torch.cuda.current_stream()
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    clean = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-    sink = torch.empty((), dtype=torch.float32, device=dev)
-
-    def flush_l2(v):
-        # write more than L2 holds, then read another buffer that size, so L2
-        # ends up holding clean lines (no write-back competes with the next op)
-        flush.fill_(v)
-        torch.sum(clean, dim=0, out=sink)
     has_store = w.has_store and w.num_tokens > 0 and attn is None
-
-    def barrier():
-        if world > 1:
-            torch.distributed.barrier()
-        torch.cuda.synchronize()
-
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
-
-    one_op = args.path in ("fused", "attention")  # no separate store op
-
-    def step(e=None):
-        if not one_op:
-            flush_l2(1)
-        if e: e[0].record(stream)
-        if has_store and not one_op:
-            d.store(stream)
-        if e: e[1].record(stream)
-        flush_l2(2)
-        if e: e[2].record(stream)
-        if attn is not None:
-            attn(stream)  # split plan + attention kernel + merge kernel
-        elif args.path == "fused":
-            d.append_gather(stream)  # plan kernel + fused append/gather kernel
-        else:
-            d.gather(stream)  # plan kernel + gather kernel (programmatic dependent launch)
-        if e: e[3].record(stream)
-
-    for _ in range(args.warmup):
-        step()
-    if d.error_code() != 0:
-        raise RuntimeError("device error during warm-up")
-    uuid = None
-    try:
-        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
-    except Exception:
-        pass
-    with ClockSampler(uuid) as clocks:
-        barrier()
-        t0 = time.perf_counter()
-        for i in range(args.steps):
-            step(ev[i])
-        barrier()
-        wall = time.perf_counter() - t0
-    st_ms = [0.0 if one_op else e[0].elapsed_time(e[1]) for e in ev]
-    ga_ms = [e[2].elapsed_time(e[3]) for e in ev]
-    step_ms = [a + b for a, b in zip(st_ms, ga_ms)]
-    if d.error_code() != 0:
-        raise RuntimeError("device error during the timed steps")
-    local = {"step_ms": float(np.mean(step_ms)), "store_ms": float(np.mean(st_ms)),
-             "gather_ms": float(np.mean(ga_ms)), "wall_s": wall}
+    timer = Timer(dev, world)
+    with ClockSampler(gpu_uuid(dev)) as clocks:
+        local = timer.run(d, attn, args.path, has_store, args.steps, args.warmup)
     local["step_ms"], local["store_ms"], local["gather_ms"] = reduce_max(
         [local["step_ms"], local["store_ms"], local["gather_ms"]], device=dev)
+
     def make_twin():
         # a second device copy of the batch for the overlapped end-to-end loop
         if args.path == "bf16":
@@ -313,7 +360,51 @@ def run_gpu(args, rank, world):
               if attn is not None else None)
         return d2, a2
     e2e = run_e2e(args, w, d, dev, nbytes, attn, make_twin) if rank == 0 else None
-    return w, nbytes, local, clocks.summary(), e2e, has_store
+    del d, attn
+    sweep = None
+    if args.path == "c8" and world == 1 and not args.no_workload_sweep:
+        sweep = run_sweep(args, w, local, timer, dev)
+    return w, nbytes, local, clocks.summary(), e2e, has_store, sweep
+
+
+def op_figures(w, nbytes, t, peak):
+    """Per-op time, GB/s (algorithmic bytes / time), fraction of peak and
+    tokens/s of one batch's store and gather."""
+    out = {}
+    if w.has_store and w.num_tokens > 0 and t["store_ms"] > 0:
+        gbs = nbytes["store"] / (t["store_ms"] * 1e-3) / 1e9
+        out["store"] = {"ms": round(t["store_ms"], 5), "GB_s": round(gbs, 1),
+                        "frac": round(gbs / peak, 4),
+                        "tokens_per_s": round(w.num_tokens / (t["store_ms"] * 1e-3), 1),
+                        "bytes": nbytes["store"]}
+    gbs = nbytes["gather"] / (t["gather_ms"] * 1e-3) / 1e9
+    out["dequant_gather"] = {"ms": round(t["gather_ms"], 5), "GB_s": round(gbs, 1),
+                             "frac": round(gbs / peak, 4),
+                             "tokens_per_s": round(w.total_context / (t["gather_ms"] * 1e-3), 1),
+                             "bytes": nbytes["gather"]}
+    return out
+
+
+def run_sweep(args, w_head, t_head, timer, dev):
+    """Store and gather of each full-size batch, timed like the headline (its
+    own warm-up, the same L2 flush and events), one batch on the device at a
+    time.  The headline batch reuses its own timing."""
+    from dequant_kvc8_store_gb300.device import DeviceBatch
+    peak, _ = measured_peak()
+    steps, warm = max(3, min(args.steps, 100)), max(3, min(args.warmup, 10))
+    out = {"steps": steps, "warmup": warm}
+    with ClockSampler(gpu_uuid(dev)) as clocks:
+        for name in SWEEP_WORKLOADS:
+            if name == args.workload:
+                out[name] = op_figures(w_head, W.algorithmic_bytes(w_head), t_head, peak)
+                continue
+            w = W.NAMED[name](seed=rank_seed(name, 0))
+            d = DeviceBatch(w, device=dev)
+            t = timer.run(d, None, "c8", w.has_store and w.num_tokens > 0, steps, warm)
+            out[name] = op_figures(w, W.algorithmic_bytes(w), t, peak)
+            del d
+    out["clocks"] = clocks.summary()
+    return out
 
 
 def run_e2e(args, w, d, dev, nbytes, attn, make_twin):
@@ -530,6 +621,12 @@ def cpu_baseline(w: W.Workload, path: str = "c8", seconds: float = 12.0,
             "sample": sample}
 
 
+def config_of(args) -> dict:
+    """The `config` object of both arms' lines (identical for the same flags)."""
+    return {"workload": WORKLOAD_TEXT[args.workload], "path": PATH_TEXT[args.path],
+            "l2": L2_TEXT}
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return
@@ -547,24 +644,24 @@ def run_reference(args, rank, world):
     times = [oracle_pass(s, args.path) for _ in range(steps)]
     ms = 1e3 * sum(times) / len(times)
     value = bytes_step / (ms * 1e-3) / 1e9
+    positions = int(s.q_lens().sum() + s.context_lengths.astype(np.int64).sum())
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
         "n_gpus": world, "steps": steps, "warmup": warm, "ms_per_step": round(ms, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if args.path == "bf16" else "f32",
-        "data": "synthetic", "config": {"workload": WORKLOAD_TEXT[args.workload],
-                                        "path": PATH_TEXT[args.path],
-                                        "sample_positions_per_step": int(s.q_lens().sum() + s.context_lengths.astype(np.int64).sum())},
+        "data": "synthetic", "config": config_of(args),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": f"each step: oracle store+gather of the first {s.num_seqs} "
-                                   f"sequences of the workload ({bytes_step / 1e6:.2f} MB algorithmic)"},
+                                   f"sequences of the workload ({positions} stored + gathered "
+                                   f"positions, {bytes_step / 1e6:.2f} MB algorithmic)"},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
 
-def result_line(args, world, w, nbytes, t, clocks, e2e, has_store):
+def result_line(args, world, w, nbytes, t, clocks, e2e, has_store, sweep=None):
     """The JSON line of the GPU arm from the measured op times (t: ms per op)."""
     peak, peak_kind = measured_peak()
     total = nbytes["store"] + nbytes["gather"]
@@ -594,6 +691,8 @@ def result_line(args, world, w, nbytes, t, clocks, e2e, has_store):
                         "note": "done inside the fused append + gather launch"}
         ops["dequant_gather"]["appended_tokens_per_s"] = round(
             w.num_tokens / (t["gather_ms"] * 1e-3), 1) if has_store else None
+    if sweep is not None:
+        ops["by_workload"] = sweep
     # the dominant kernel: the op with the larger device time
     dom = "dequant_gather" if (t["gather_ms"] >= t["store_ms"] or not timed_store) else "store"
     dom_bytes = nbytes["gather"] if dom == "dequant_gather" else nbytes["store"]
@@ -615,18 +714,17 @@ def result_line(args, world, w, nbytes, t, clocks, e2e, has_store):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if args.path == "bf16" else "f32",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD_TEXT[args.workload],
-                   "path": PATH_TEXT[args.path],
-                   "l2": "flushed before each timed op (256 MiB write, then 256 MiB read)",
-                   "hbm_frac_of_step": round(total / (t["step_ms"] * 1e-3) / 1e9 / peak, 4),
-                   "tokens_per_s": ({"decode_attention": ops["decode_attention"]["positions_per_s"]}
-                                    if attention else
-                                    {"store": ops["store"]["tokens_per_s"],
-                                     "dequant_gather": ops["dequant_gather"]["tokens_per_s"]})},
+        "config": config_of(args),
+        "hbm_frac_of_step": round(total / (t["step_ms"] * 1e-3) / 1e9 / peak, 4),
+        "tokens_per_s": ({"decode_attention": ops["decode_attention"]["positions_per_s"]}
+                         if attention else
+                         {"store": ops["store"]["tokens_per_s"],
+                          "dequant_gather": ops["dequant_gather"]["tokens_per_s"]}),
         "ops": ops,
         "roofline": {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "peak_kind": peak_kind, "traffic": traffic,
+                     "dram_frac": ncu_dram_frac(args.workload, kname + "_kernel", peak),
                      "algorithmic_bytes": dom_bytes},
         # fused: plan + fused kernel, or store + plan + gather for a long append
         "gpu_launches": args.steps * (3 if (has_store and not fused) or attention or
@@ -646,13 +744,16 @@ def main():
     ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["kvc8", "reference"], default="kvc8")
-    ap.add_argument("--workload", choices=list(W.NAMED), default="prefill")
+    ap.add_argument("--workload", choices=list(W.NAMED), default=DEFAULT_WORKLOAD)
     ap.add_argument("--path", choices=["c8", "bf16", "fused", "attention"], default="c8",
                     help="c8: the int8 cache (default); bf16: the cache without quantisation; "
                          "fused: the int8 store and gather as one append + gather pass; "
                          "attention: decode attention (4 query heads per kv head) read "
                          "straight from the int8 cache")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workload-sweep", action="store_true",
+                    help="int8 path on one GPU: do not also time the prefill, decode, mixed "
+                         "and long-context batches")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -665,9 +766,9 @@ def main():
         import torch
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
         torch.distributed.init_process_group("nccl")
-    w, nbytes, t, clocks, e2e, has_store = run_gpu(args, rank, world)
+    w, nbytes, t, clocks, e2e, has_store, sweep = run_gpu(args, rank, world)
     if rank == 0:
-        line = result_line(args, world, w, nbytes, t, clocks, e2e, has_store)
+        line = result_line(args, world, w, nbytes, t, clocks, e2e, has_store, sweep)
         if world == 1 and not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(w, args.path)
         print(json.dumps(line), flush=True)

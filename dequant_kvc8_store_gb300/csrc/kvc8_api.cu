@@ -10,14 +10,18 @@
 namespace kvc8 {
 
 int sm_count() {
-    static int cached[64];
+    static std::atomic<int> cached[kMaxDevices];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 1;
-    if (dev < 64 && cached[dev] > 0) return cached[dev];
+    const bool in_range = dev >= 0 && dev < kMaxDevices;
+    if (in_range) {
+        const int c = cached[dev].load(std::memory_order_relaxed);
+        if (c > 0) return c;
+    }
     int n = 0;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
         n = 1;
-    if (dev < 64) cached[dev] = n;
+    if (in_range) cached[dev].store(n, std::memory_order_relaxed);
     return n;
 }
 
@@ -32,6 +36,16 @@ constexpr int64_t kFusedAppendMaxRows = 16384;
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+kvc8_status cuda_status(cudaError_t e) { return e == cudaSuccess ? KVC8_OK : KVC8_ERR_CUDA; }
+
+kvc8_status check_workspace(const kvc8_geom *g, const void *ws, size_t bytes) {
+    if (ws == nullptr || !aligned(ws, kAlign)) return KVC8_ERR_WORKSPACE;
+    if (bytes < plan_bytes(g->num_seqs)) return KVC8_ERR_WORKSPACE;
+    return KVC8_OK;
+}
+
+}  // namespace
+
 kvc8_status check_geom(const kvc8_geom *g) {
     if (g == nullptr) return KVC8_ERR_INVALID_ARG;
     if (g->num_seqs < 0 || g->kv_heads < 1 || g->block_size < 1 || g->num_blocks < 1 ||
@@ -42,14 +56,6 @@ kvc8_status check_geom(const kvc8_geom *g) {
     if (g->head_dim > kMaxHeadDim) return KVC8_ERR_UNSUPPORTED;
     // tile and unit counters are 32/64-bit; keep B * MB * 2H well inside int64
     if ((int64_t)g->num_seqs * g->max_blocks_per_seq > (int64_t)INT32_MAX) return KVC8_ERR_UNSUPPORTED;
-    return KVC8_OK;
-}
-
-kvc8_status cuda_status(cudaError_t e) { return e == cudaSuccess ? KVC8_OK : KVC8_ERR_CUDA; }
-
-kvc8_status check_workspace(const kvc8_geom *g, const void *ws, size_t bytes) {
-    if (ws == nullptr || !aligned(ws, kAlign)) return KVC8_ERR_WORKSPACE;
-    if (bytes < plan_bytes(g->num_seqs)) return KVC8_ERR_WORKSPACE;
     return KVC8_OK;
 }
 
@@ -68,7 +74,6 @@ kvc8_status check_gather_args(const kvc8_geom *g, const int8_t *kc, const int8_t
     return KVC8_OK;
 }
 
-}  // namespace
 }  // namespace kvc8
 
 using namespace kvc8;

@@ -456,25 +456,17 @@ cudaError_t launch_attention_variant(const AttnArgs &a, cudaStream_t stream) {
     auto kern = attention_kernel<MODE, D>;
     const size_t smem = sizeof(float) * ((MODE == 1 ? 2 * a.g.kv_heads * (D + 16) : 0) +
                                          kAttnWarps * kMaxGroup * (D + 2));
-    static int cached_dev = -1;
-    static size_t cached_smem = 0;
-    static int cached_occ = 0;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
+    static OccupancySlots slots;
+    cudaError_t e = cudaSuccess;
     if (smem > 48 * 1024) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
     }
-    if (cached_dev != dev || cached_smem != smem) {
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&cached_occ, kern, kAttnThreads, smem);
-        if (e != cudaSuccess) return e;
-        if (cached_occ < 1) cached_occ = 1;
-        cached_dev = dev;
-        cached_smem = smem;
-    }
+    int occ = 0;
+    e = occupancy(slots, kern, kAttnThreads, smem, &occ);
+    if (e != cudaSuccess) return e;
     const int64_t max_items = (int64_t)part_elems(a.g);
-    const int64_t cap = (int64_t)sm_count() * cached_occ;
+    const int64_t cap = (int64_t)sm_count() * occ;
     const int grid = (int)(max_items < cap ? max_items : cap);
     if (grid <= 0) return cudaSuccess;
     cudaLaunchConfig_t cfg = {};

@@ -238,19 +238,12 @@ cudaError_t launch_store_bf16(const StoreBf16Args &a, cudaStream_t stream) {
     const bool wide = a32(a.k_states) && a32(a.v_states) && a32(a.k_cache) && a32(a.v_cache) &&
                       a.x_tok_stride % 16 == 0 && a.x_head_stride % 16 == 0;
     auto kern = wide ? store_bf16_kernel<true> : store_bf16_kernel<false>;
-    static int cached_dev[2] = {-1, -1}, cached_occ[2] = {0, 0};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    static OccupancySlots slots[2];
+    int occ = 0;
+    const cudaError_t e = occupancy(slots[wide], kern, kWarpsPerCta * 32, 0, &occ);
     if (e != cudaSuccess) return e;
-    if (cached_dev[wide] != dev) {
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&cached_occ[wide], kern,
-                                                          kWarpsPerCta * 32, 0);
-        if (e != cudaSuccess) return e;
-        if (cached_occ[wide] < 1) cached_occ[wide] = 1;
-        cached_dev[wide] = dev;
-    }
     const int64_t need = (a.num_tokens + kWarpsPerCta - 1) / kWarpsPerCta;
-    const int64_t cap = (int64_t)sm_count() * cached_occ[wide];
+    const int64_t cap = (int64_t)sm_count() * occ;
     kern<<<(int)(need < cap ? need : cap), kWarpsPerCta * 32, 0, stream>>>(a);
     return cudaGetLastError();
 }
@@ -260,18 +253,12 @@ cudaError_t launch_gather_bf16(const GatherBf16Args &a, bool use_pdl, cudaStream
     const bool wide = a32(a.k_cache) && a32(a.v_cache) && a32(a.k_out) && a32(a.v_out) &&
                       a.out_tok_stride % 16 == 0 && a.out_head_stride % 16 == 0;
     auto kern = wide ? gather_bf16_kernel<true> : gather_bf16_kernel<false>;
-    static int cached_dev[2] = {-1, -1}, cached_occ[2] = {0, 0};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    static OccupancySlots slots[2];
+    int occ = 0;
+    const cudaError_t e = occupancy(slots[wide], kern, kGatherThreads, 0, &occ);
     if (e != cudaSuccess) return e;
-    if (cached_dev[wide] != dev) {
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&cached_occ[wide], kern, kGatherThreads, 0);
-        if (e != cudaSuccess) return e;
-        if (cached_occ[wide] < 1) cached_occ[wide] = 1;
-        cached_dev[wide] = dev;
-    }
     const int64_t max_items = (int64_t)a.g.num_seqs * a.g.max_blocks_per_seq * a.g.kv_heads;
-    const int64_t cap = (int64_t)sm_count() * cached_occ[wide];
+    const int64_t cap = (int64_t)sm_count() * occ;
     const int grid = (int)(max_items < cap ? max_items : cap);
     if (grid <= 0) return cudaSuccess;
     cudaLaunchConfig_t cfg = {};

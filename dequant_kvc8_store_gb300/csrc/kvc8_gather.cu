@@ -485,27 +485,15 @@ cudaError_t launch_gather_variant(const GatherArgs &a, const AppendArgs &p, bool
                                   cudaStream_t stream) {
     auto kern = gather_kernel<MODE, CH, WIDE, APPEND>;
     const size_t smem = MODE == 1 ? sizeof(float) * 2 * a.g.kv_heads * (a.g.head_dim / CH) * (CH + 4) : 0;
-    static int cached_dev = -1;
-    static size_t cached_smem = 0;
-    static int cached_occ = 0;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
+    static OccupancySlots slots;
+    cudaError_t e = cudaSuccess;
     if (smem > 48 * 1024) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
     }
     int occ = 0;
-    if (cached_dev == dev && cached_smem == smem) {
-        occ = cached_occ;
-    } else {
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kGatherThreads, smem);
-        if (e != cudaSuccess) return e;
-        if (occ < 1) occ = 1;
-        cached_occ = occ;
-        cached_smem = smem;
-        cached_dev = dev;
-    }
+    e = occupancy(slots, kern, kGatherThreads, smem, &occ);
+    if (e != cudaSuccess) return e;
     const int64_t max_items = (int64_t)a.g.num_seqs * a.g.max_blocks_per_seq * a.g.kv_heads +
                               (APPEND ? p.items : 0);
     const int64_t cap = (int64_t)sm_count() * occ;

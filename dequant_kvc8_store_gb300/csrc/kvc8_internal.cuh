@@ -2,6 +2,7 @@
 // libkvc8 translation units (store, gather, C ABI).  Not part of the ABI.
 #pragma once
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 
@@ -310,5 +311,47 @@ cudaError_t reset_plan_counter(void *plan, cudaStream_t stream);
 
 // Per-device SM count (cached).
 int sm_count();
+
+// Host-side caches of per-device launch facts.  Each is one atomic word per
+// device, so host threads that launch at the same time -- on one device or on
+// several -- read either a complete entry or none (and then query again).
+constexpr int kMaxDevices = 64;
+
+struct OccupancySlots {
+    std::atomic<uint64_t> word[kMaxDevices];  // ((smem + 1) << 8) | CTAs per SM; 0 = unknown
+};
+
+// Resident CTAs per SM of `kern` with `threads` threads and `smem` bytes of
+// dynamic shared memory on the current device, cached in `slots` (one
+// OccupancySlots per kernel variant).
+template <typename Kernel>
+cudaError_t occupancy(OccupancySlots &slots, Kernel kern, int threads, size_t smem, int *occ) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const bool cached = dev >= 0 && dev < kMaxDevices;
+    const uint64_t key = ((uint64_t)smem + 1) << 8;
+    if (cached) {
+        const uint64_t w = slots.word[dev].load(std::memory_order_relaxed);
+        if ((w & ~(uint64_t)0xFF) == key) {
+            *occ = (int)(w & 0xFF);
+            return cudaSuccess;
+        }
+    }
+    int n = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, threads, smem);
+    if (e != cudaSuccess) return e;
+    n = n < 1 ? 1 : (n > 255 ? 255 : n);
+    if (cached) slots.word[dev].store(key | (uint64_t)n, std::memory_order_relaxed);
+    *occ = n;
+    return cudaSuccess;
+}
+
+// Host-side argument checks shared by the entry points (kvc8_api.cu).
+kvc8_status check_geom(const kvc8_geom *g);
+kvc8_status check_gather_args(const kvc8_geom *g, const int8_t *kc, const int8_t *vc,
+                              const float *ks, const float *vs, const int32_t *bt,
+                              const int32_t *lens, const void *ko, const void *vo,
+                              int64_t out_rows, int64_t tok_stride, int64_t head_stride);
 
 }  // namespace kvc8

@@ -31,7 +31,6 @@ constexpr size_t kNoallocScratchBytes =
 
 static __device__ __align__(256) unsigned char g_gather_scratch[kNoallocScratchBytes];
 
-constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mutex;
 void *g_scratch_ptr[kMaxDevices];
 
@@ -63,29 +62,20 @@ extern "C" kvc8_status kvc8_dequant_gather_noalloc(
     const int32_t *context_lengths, const int64_t *context_seq_offset, void *key_out,
     void *value_out, int64_t out_rows, int64_t out_tok_stride, int64_t out_head_stride,
     int32_t *dev_error, cudaStream_t stream) {
-    // Same checks as kvc8_dequant_gather, then the size limit of the array.
-    if (g == nullptr || g->num_seqs < 0 || g->kv_heads < 1 || g->block_size < 1 ||
-        g->num_blocks < 1 || g->max_blocks_per_seq < 1 || g->head_dim < 16 ||
-        g->head_dim % 16 != 0 || (g->quant_mode != 0 && g->quant_mode != 1))
-        return KVC8_ERR_INVALID_ARG;
-    if (g->head_dim > 256) return KVC8_ERR_UNSUPPORTED;
-    if (g->num_seqs > KVC8_NOALLOC_MAX_SEQS) return KVC8_ERR_UNSUPPORTED;
-    if (g->num_seqs == 0) return KVC8_OK;
-    if (key_cache == nullptr || value_cache == nullptr || key_scale == nullptr ||
-        value_scale == nullptr || block_table == nullptr || context_lengths == nullptr ||
-        key_out == nullptr || value_out == nullptr)
-        return KVC8_ERR_INVALID_ARG;
-    if (out_rows < 0 || out_tok_stride < 0 || out_head_stride < 0 || out_tok_stride % 8 != 0 ||
-        out_head_stride % 8 != 0)
-        return KVC8_ERR_INVALID_ARG;
-    auto misaligned = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) != 0; };
-    if (misaligned(key_out) || misaligned(value_out) || misaligned(key_cache) ||
-        misaligned(value_cache) || misaligned(key_scale) || misaligned(value_scale))
-        return KVC8_ERR_INVALID_ARG;
-    if (plan_bytes(g->num_seqs) > kNoallocScratchBytes) return KVC8_ERR_UNSUPPORTED;
-
+    // The checks of kvc8_dequant_gather, then the size limit of the array.
+    kvc8_status st = check_geom(g);
+    if (st != KVC8_OK) return st;
+    if (g->num_seqs > KVC8_NOALLOC_MAX_SEQS || plan_bytes(g->num_seqs) > kNoallocScratchBytes)
+        return KVC8_ERR_UNSUPPORTED;
+    // The set-up comes before the early return, so that a call with
+    // num_seqs = 0 at start-up prepares the device without doing any work.
     void *scratch = nullptr;
     if (scratch_for_current_device(&scratch) != cudaSuccess) return KVC8_ERR_CUDA;
+    if (g->num_seqs == 0) return KVC8_OK;
+    st = check_gather_args(g, key_cache, value_cache, key_scale, value_scale, block_table,
+                           context_lengths, key_out, value_out, out_rows, out_tok_stride,
+                           out_head_stride);
+    if (st != KVC8_OK) return st;
     if (launch_plan(*g, context_lengths, context_seq_offset, nullptr, scratch, dev_error,
                     stream) != cudaSuccess)
         return KVC8_ERR_CUDA;

@@ -436,37 +436,21 @@ store_kernel(const StoreArgs a) {
     }
 }
 
-struct OccCache {
-    int dev = -1;
-    size_t smem = 0;
-    int occ = 0;
-};
-
 template <int E, int LANES, int MODE, bool V32>
 cudaError_t launch_variant(const StoreArgs &a, cudaStream_t stream) {
     auto kern = store_kernel<E, LANES, MODE, V32>;
     const int C = a.g.head_dim / E;
     const size_t smem = MODE == 1 ? sizeof(float) * 2 * a.g.kv_heads * C * (E + 2)
                         : MODE == 0 ? sizeof(float) * 256 : 0;
-    static OccCache cache;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
+    static OccupancySlots slots;
+    cudaError_t e = cudaSuccess;
     if (smem > 48 * 1024) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
     }
     int occ = 0;
-    if (cache.dev == dev && cache.smem == smem) {
-        occ = cache.occ;
-    } else {
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kWarpsPerCta * 32, smem);
-        if (e != cudaSuccess) return e;
-        if (occ < 1) occ = 1;
-        cache.occ = occ;
-        cache.smem = smem;
-        cache.dev = dev;
-    }
+    e = occupancy(slots, kern, kWarpsPerCta * 32, smem, &occ);
+    if (e != cudaSuccess) return e;
     const int64_t need = (a.num_tokens + kWarpsPerCta - 1) / kWarpsPerCta;
     const int64_t cap = (int64_t)sm_count() * occ;
     const int grid = (int)(need < cap ? need : cap);

@@ -418,15 +418,24 @@ kvc8_status kvc8_gather_bf16(const kvc8_geom *g, const void *key_cache,
  * KVC8_NOALLOC_MAX_SEQS is rejected with KVC8_ERR_UNSUPPORTED before anything
  * is enqueued.
  *
- * The first call on a device looks up that device's copy of the array
- * (cudaGetSymbolAddress, with the device current) and remembers it; make that
- * first call before any stream capture.  All calls on a device share the
- * array: each call rewrites everything it reads from it, but calls whose work
- * overlaps on the GPU (other streams, other host threads) race on it and must
- * be serialised by the caller.
+ * Set-up: the first call on a device looks up that device's copy of the array
+ * (cudaGetSymbolAddress, with the device current) and remembers it.  With
+ * lazy module loading, that lookup is also when the library's device code and
+ * globals -- this array included -- are loaded onto the device, which
+ * allocates device memory; and each kernel's code is loaded at its first
+ * launch.  So make the first call on each device at start-up, before any
+ * stream capture and before the phase that must not allocate: a call with
+ * g->num_seqs = 0 does the lookup and nothing else, and one call on a small
+ * real batch also loads the plan and gather kernels.
  *
- * Arguments, layouts and results are those of kvc8_dequant_gather, without
- * the workspace pair.
+ * Sharing: all calls on a device use the one array.  Each call rewrites every
+ * field it reads from it (the plan kernel zeroes the work counter), but calls
+ * whose work overlaps on the GPU (other streams, other host threads) race on
+ * it and must be serialised by the caller.
+ *
+ * Arguments, checks, layouts and results are those of kvc8_dequant_gather in
+ * every quant_mode (0, 1 and 2), without the workspace pair; the same
+ * geometries are refused, plus num_seqs above KVC8_NOALLOC_MAX_SEQS.
  */
 kvc8_status kvc8_dequant_gather_noalloc(const kvc8_geom *g, const int8_t *key_cache,
                                         const int8_t *value_cache,

@@ -13,6 +13,14 @@ KEYS = {"metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
         "roofline", "gpu_launches", "clocks", "e2e"}
 
 
+def test_default_workload_is_the_decode_batch():
+    ap_default = bench.DEFAULT_WORKLOAD
+    assert ap_default == "decode"
+    w = W.decode()
+    # the largest batch that runs both ops: a store and a gather of > 1 M positions
+    assert w.has_store and w.num_tokens == 256 and w.total_context > 1_000_000
+
+
 @pytest.mark.parametrize("path", ["c8", "bf16", "fused", "attention"])
 @pytest.mark.parametrize("gather_only", [False, True])
 def test_result_line_for_every_path(path, gather_only):
@@ -35,6 +43,33 @@ def test_result_line_for_every_path(path, gather_only):
         assert line["gpu_launches"] == 7 * (2 if one_op or gather_only else 3)
     if path == "fused":
         assert line["ops"]["store"]["ms"] == 0.0
+    assert line["config"] == bench.config_of(args)
+
+
+def test_result_line_carries_the_workload_sweep():
+    w = W.tiny()
+    args = argparse.Namespace(path="c8", workload="tiny", steps=7, warmup=3)
+    t = {"step_ms": 0.05, "store_ms": 0.02, "gather_ms": 0.03, "wall_s": 1.0}
+    peak, _ = bench.measured_peak()
+    sweep = {"steps": 7, "warmup": 3, "clocks": {"sm_mhz": 2070.0}}
+    for name in bench.SWEEP_WORKLOADS:
+        sweep[name] = bench.op_figures(w, bench.path_bytes(w, "c8"), t, peak)
+    line = bench.result_line(args, 1, w, bench.path_bytes(w, "c8"), t, {}, None, True, sweep)
+    json.dumps(line)
+    by = line["ops"]["by_workload"]
+    for name in bench.SWEEP_WORKLOADS:
+        for op in ("store", "dequant_gather"):
+            e = by[name][op]
+            assert e["ms"] > 0 and e["GB_s"] > 0 and 0 < e["frac"] and e["tokens_per_s"] > 0
+
+
+def test_reference_arm_prints_the_same_config(capsys):
+    args = argparse.Namespace(path="c8", workload="tiny", steps=3, warmup=3)
+    bench.run_reference(args, 0, 1)
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference"
+    assert line["config"] == bench.config_of(args)
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["value"] == line["value"]
 
 
 def test_traffic_entries_follow_their_kernel_sources(tmp_path, monkeypatch):
@@ -61,6 +96,24 @@ def test_traffic_entries_follow_their_kernel_sources(tmp_path, monkeypatch):
     assert bench.ncu_traffic("prefill", "gather_kernel") is None
 
 
+def test_dram_fraction_from_the_captured_launch(tmp_path, monkeypatch):
+    root = tmp_path
+    csrc = root / "dequant_kvc8_store_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    for f in ("kvc8_gather.cu", "kvc8_internal.cuh"):
+        (csrc / f).write_text(f"// {f}\n")
+    monkeypatch.setattr(bench, "ROOT", str(root))
+    (root / "profiles").mkdir()
+    e = {"bytes": 4000, "captured_on": "decode_small", "captured_bytes": 1000,
+         "captured_ns": 1000.0, "source_hash": bench.kernel_hash("gather_kernel")}
+    (root / "profiles" / "ncu_traffic.json").write_text(
+        json.dumps({"workloads": {"decode": {"gather_kernel": e}}}))
+    # 1000 bytes in 1 us = 1 GB/s
+    assert bench.ncu_dram_frac("decode", "gather_kernel", 2.0) == 0.5
+    assert bench.ncu_traffic("decode", "gather_kernel") == 4000
+    assert bench.ncu_dram_frac("decode", "store_kernel", 2.0) is None
+
+
 def test_committed_traffic_file_is_well_formed():
     with open(bench.os.path.join(bench.ROOT, "profiles", "ncu_traffic.json")) as f:
         d = json.load(f)
@@ -69,3 +122,6 @@ def test_committed_traffic_file_is_well_formed():
         for k, e in ks.items():
             assert k in bench.KERNEL_FILES
             assert int(e["bytes"]) > 0 and len(e["source_hash"]) == 16
+            if "captured_ns" in e:
+                assert int(e["captured_bytes"]) > 0 and float(e["captured_ns"]) > 0
+                assert e["captured_on"] in W.NAMED
