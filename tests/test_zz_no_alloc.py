@@ -68,7 +68,7 @@ def test_noalloc_gather_matches_oracle_and_workspace_gather_in_a_row():
                              with_store=False)
     third = W.make_workload("noalloc-c", q_lens=np.zeros(7, np.int64),
                             ctx_before=[33, 0, 250, 1, 16, 17, 99], kv_heads=4, head_dim=128,
-                            block_size=16, num_blocks=60, quant_mode=2, seed=406,
+                            block_size=16, num_blocks=120, quant_mode=2, seed=406,
                             with_store=False)
     _check_against_oracle_and_workspace_gather(first)
     lens = second.context_lengths.astype(np.int64)
