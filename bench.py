@@ -442,8 +442,8 @@ def run_e2e(args, w, d, dev, nbytes, attn, make_twin):
                  torch.empty(d.v_out.shape, dtype=torch.bfloat16).pin_memory()) for _ in range(2)]
         h2d = sum(t.numel() * t.element_size() for t in host.values())
         d2h = outs[0][0].numel() * 2 * 2
-    # bounded: at most ~16 GB of host<->device traffic, at least 3 steps
-    steps = max(3, min(args.steps, 50, int(16e9 // max(1, h2d + d2h))))
+    # bounded: at most ~32 GB of host<->device traffic, at least 3 steps
+    steps = max(3, min(args.steps, 50, int(32e9 // max(1, h2d + d2h))))
     ev_in = [torch.cuda.Event() for _ in range(2)]
     ev_comp = [torch.cuda.Event() for _ in range(2)]
     ev_out = [torch.cuda.Event() for _ in range(2)]

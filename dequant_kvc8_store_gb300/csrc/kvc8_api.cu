@@ -28,7 +28,9 @@ int sm_count() {
 namespace {
 
 constexpr int kMaxHeadDim = 256;
-constexpr int64_t kMaxStaticTable = 12288;  // kv_heads * head_dim, mode-1 store shared memory
+// kv_heads * head_dim of a mode-1 store: its per-channel table (bracket ends and
+// clamp bounds, about 11 bytes per K and V channel) lives in shared memory
+constexpr int64_t kMaxStaticTable = 8192;
 // Appended rows (tokens x 2 x kv_heads) up to which the fused append + gather
 // beats the store followed by a gather (measured on decode-shaped batches:
 // 16 384 rows still won, 65 536 lost).

@@ -50,6 +50,18 @@ constexpr int kWarpsPerCta = 8;
 constexpr float kMagic = 12582912.0f;            // 1.5 * 2^23
 constexpr float kNearTie = 0.499969482421875f;   // 0.5 - 2^-15
 constexpr float kSatClamp = 127.0f;   // |y| >= 127 gives +-127 on both paths
+constexpr float kRecipLo = 0.99999952316284180f;  // 1 - 2^-21
+constexpr float kRecipHi = 1.00000047683715820f;  // 1 + 2^-21
+
+// The clamp bound of a static scale s (recip_ok(s)): B = bf16_rne(fl(127 s)).
+// B / s lies within a relative 2^-8 + 2^-24 of 127, i.e. in (126.5, 127.5),
+// so rne(fl(B / s)) = 127, and by monotonicity every |x| >= B has a code of
+// at least 127 in magnitude: clamping |x| to B leaves clamp(code(x)) unchanged.
+__device__ __forceinline__ uint32_t bf16_bound(float s) {
+    unsigned short b;
+    asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(b) : "f"(__fmul_rn(127.0f, s)));
+    return b;
+}
 
 // Reciprocal fast path needs s and 1/s normal and finite.
 __device__ __forceinline__ bool recip_ok(float s) {
@@ -115,11 +127,11 @@ __device__ __forceinline__ uint32_t pack_lo_bytes(uint32_t a, uint32_t b, uint32
 
 // The groups of four codes flagged in `fix` (bit q: codes 4q..4q+3 of a
 // lane's run), recomputed from the source values one by one with the exact
-// fallback and stored over the fast codes at dst.  Mode 1 reads each value's
-// scale and reciprocal; modes 0 and 2 use the row's.
+// fallback and stored over the fast codes at dst.  Mode 1 divides by each
+// value's scale; modes 0 and 2 use the row's scale and reciprocal.
 template <int MODE>
 __device__ __noinline__ void fix_codes(const uint16_t *src, int8_t *dst, uint32_t fix, float s_row,
-                                       float r_row, const float *st, const float *rt) {
+                                       float r_row, const float *st) {
     while (fix != 0u) {
         const int q = __ffs(fix) - 1;
         fix &= fix - 1u;
@@ -128,7 +140,7 @@ __device__ __noinline__ void fix_codes(const uint16_t *src, int8_t *dst, uint32_
         for (int e = 0; e < 4; ++e) {
             const int j = 4 * q + e;
             const float x = __uint_as_float((uint32_t)src[j] << 16);
-            const int code = MODE == 1 ? quant_one(x, ld_nc_f32(st + j), rt[j]) : quant_one(x, s_row, r_row);
+            const int code = MODE == 1 ? quant_exact(x, ld_nc_f32(st + j)) : quant_one(x, s_row, r_row);
             c4[e] = (uint32_t)code;
         }
         *reinterpret_cast<uint32_t *>(dst + 4 * q) = pack_lo_bytes(c4[0], c4[1], c4[2], c4[3]);
@@ -192,15 +204,20 @@ store_kernel(const StoreArgs a) {
     // Shared tables.  Dynamic mode: for a bf16 row maximum amax = (1 + m/128)
     // * 2^E, s = fl(amax / 127) = fl((1 + m/128) / 127) * 2^E and
     // 1/s rounds to fl(1 / that) * 2^-E exactly, as long as both stay normal;
-    // the tables hold the two fl() values for the 128 mantissas.  Static mode:
-    // the reciprocal table [2][H][D], stored as chunks of E values (one per
-    // lane and row) padded by 2 floats so that the 32 lanes of a warp read
-    // different banks; a zero reciprocal marks a scale that must take the exact
-    // path (which reads the scale itself from global memory).
+    // the tables hold the two fl() values for the 128 mantissas.  Static
+    // per-channel mode: for each (K|V, head, channel) the bracket ends r_lo,
+    // r_hi of r = fl(1/s) (as float4 {r_lo, r_lo', r_hi, r_hi'} per pair of
+    // channels, one chunk of E channels per lane and row, padded by 4 floats)
+    // and the clamp bound bf16(fl(127 s)) (a chunk of E bf16 per lane and row,
+    // padded by 8), laid out so that the 8 lanes of each shared-memory
+    // wavefront read different banks.  A scale outside the reciprocal range
+    // sends the whole launch to the exact path.
     extern __shared__ float smem[];
     float *s_tab = smem;                           // dynamic mode only
     float *r_tab = smem + (MODE == 0 ? 128 : 0);
-    constexpr int CHUNK = E + 2;                   // padded chunk stride (static mode)
+    constexpr int RCH = 2 * E + 4;                 // floats per (row, lane) chunk, static mode
+    constexpr int BCH = E + 8;                     // bf16 per (row, lane) chunk, static mode
+    uint16_t *b_tab = reinterpret_cast<uint16_t *>(smem + 2 * H * C * RCH);
     bool all_fast = true;
     if (MODE == 0) {
         for (int m = threadIdx.x; m < 128; m += blockDim.x) {
@@ -211,11 +228,16 @@ store_kernel(const StoreArgs a) {
         __syncthreads();
     } else if (MODE == 1) {
         int ok = 1;
-        for (int i = threadIdx.x; i < 2 * H * D; i += blockDim.x) {
-            const float sc = i < H * D ? ld_nc_f32(a.k_scale + i) : ld_nc_f32(a.v_scale + (i - H * D));
+        for (int idx = threadIdx.x; idx < 2 * H * D; idx += blockDim.x) {
+            const float sc = idx < H * D ? ld_nc_f32(a.k_scale + idx) : ld_nc_f32(a.v_scale + (idx - H * D));
             const bool f = recip_ok(sc);
-            const int row = i / D, d = i - row * D;
-            r_tab[(row * C + d / E) * CHUNK + d % E] = f ? __frcp_rn(sc) : 0.0f;
+            const float r = f ? __frcp_rn(sc) : 0.0f;
+            const int row = idx / D, d = idx - row * D;
+            const int chunk = row * C + d / E, e = d % E;
+            float *rp = r_tab + chunk * RCH + (e >> 1) * 4 + (e & 1);
+            rp[0] = __fmul_rn(r, kRecipLo);
+            rp[2] = __fmul_rn(r, kRecipHi);
+            b_tab[chunk * BCH + e] = bf16_bound(sc);
             ok &= f;
         }
         all_fast = __syncthreads_and(ok) != 0;
@@ -338,54 +360,65 @@ store_kernel(const StoreArgs a) {
                 const int kv = row >= H;
                 const int h = row - kv * H;
                 const float s_row = s_rows[k], r_row = r_rows[k];
-                const float *rt = r_tab + ((kv * H + h) * C + c) * CHUNK;                // static mode
-                const float *st = (kv ? a.v_scale : a.k_scale) + (int64_t)h * D + c * E;  // static mode
+                // (lanes off the row read chunk 0: in bounds, their codes unused)
+                const int chunk = on ? (kv * H + h) * C + c : 0;
+                const float *rt = r_tab + chunk * RCH;                                   // mode 1
+                const uint16_t *bt = b_tab + chunk * BCH;                                // mode 1
+                const float *st = (kv ? a.v_scale : a.k_scale) + (int64_t)h * D + c * E;  // mode 1
 
                 uint32_t cw[W / 2];  // packed codes, four per word
                 uint32_t fix = 0u;   // bit q: codes 4q..4q+3 need the exact path
                 const bool force_exact = (MODE == 1) ? !all_fast : (r_row == 0.0f);
-                // Dynamic mode: r_lo <= r (1 - 2^-23) and r_hi >= r (1 + 2^-23)
-                // bracket every value fl(x / s) can take, so when x r_lo and
-                // x r_hi round to the same integer, so does fl(x / s).
-                const float2 rlo2 = make_float2(__fmul_rn(r_row, 0.99999952316284180f),
-                                                __fmul_rn(r_row, 0.99999952316284180f));
-                const float2 rhi2 = make_float2(__fmul_rn(r_row, 1.00000047683715820f),
-                                                __fmul_rn(r_row, 1.00000047683715820f));
+                // r_lo <= r (1 - 2^-23) and r_hi >= r (1 + 2^-23) bracket every
+                // value fl(x / s) can take, so when x r_lo and x r_hi round to
+                // the same integer, so does fl(x / s).  Modes 0 and 2: the row's
+                // pair; mode 1: each channel's, from the table.
+                const float2 rlo2 = make_float2(__fmul_rn(r_row, kRecipLo), __fmul_rn(r_row, kRecipLo));
+                const float2 rhi2 = make_float2(__fmul_rn(r_row, kRecipHi), __fmul_rn(r_row, kRecipHi));
+                // Modes 1 and 2 clamp x to +-bf16(fl(127 s)) before the bracket
+                // (one min.xorsign.abs per pair): that bound's code is +-127
+                // and every larger |x| saturates, so the clamp gives
+                // clamp(code(x)) and keeps |x r| below 127.5.
+                const uint32_t brow = MODE == 2 ? bf16_bound(s_row) * 0x10001u : 0u;
+                // Group q of four values adds its bracket gap (0 to 4, the
+                // squared differences of the ends) times 8^q to flagsf: an exact
+                // base-8 record of the flagged groups, kept on the FMA pipe.
+                float flagsf = 0.0f;
 #pragma unroll
                 for (int i = 0; i < W; i += 2) {
                     uint32_t mbits[4];
                     float2 dacc = make_float2(0.0f, 0.0f);
-                    float dm = 0.0f;
+                    uint2 b2 = make_uint2(brow, brow);
+                    if (MODE == 1) b2 = *reinterpret_cast<const uint2 *>(bt + 2 * i);
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
-                        const uint32_t wi = w[k][i + e];
-                        const float2 x2 = make_float2(__uint_as_float(wi << 16), __uint_as_float(wi & 0xFFFF0000u));
-                        float2 m2;
-                        if (MODE == 0) {
-                            m2 = __ffma2_rn(x2, rlo2, magic2);
-                            const float2 h2 = __ffma2_rn(x2, rhi2, magic2);
-                            // the two ends differ by a small integer or not at all;
-                            // their squared differences add up exactly, on the
-                            // FMA pipe rather than the busier ALU pipe
-                            const float2 dd = __fadd2_rn(h2, make_float2(-m2.x, -m2.y));
-                            dacc = __ffma2_rn(dd, dd, dacc);
-                        } else {
-                            const float2 r2 = MODE == 2 ? make_float2(r_row, r_row)
-                                              : on ? *reinterpret_cast<const float2 *>(rt + 2 * (i + e))
-                                                   : make_float2(1.0f, 1.0f);
-                            float2 y2 = __fmul2_rn(x2, r2);
-                            y2.x = fminf(fmaxf(y2.x, -kSatClamp), kSatClamp);
-                            y2.y = fminf(fmaxf(y2.y, -kSatClamp), kSatClamp);
-                            m2 = __fadd2_rn(y2, magic2);
-                            const float2 d2 = __ffma2_rn(__fadd2_rn(m2, nmagic2), neg1, y2);  // y - rne(y), exact
-                            dm = fmaxf(dm, fmaxf(fabsf(d2.x), fabsf(d2.y)));
+                        uint32_t wi = w[k][i + e];
+                        float2 rlo = rlo2, rhi = rhi2;
+                        if (MODE == 1) {
+                            const float4 r4 = *reinterpret_cast<const float4 *>(rt + 4 * (i + e));
+                            rlo = make_float2(r4.x, r4.y);
+                            rhi = make_float2(r4.z, r4.w);
                         }
+                        if (MODE != 0)
+                            asm("min.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(wi) : "r"(wi), "r"(e ? b2.y : b2.x));
+                        const float2 x2 = make_float2(__uint_as_float(wi << 16), __uint_as_float(wi & 0xFFFF0000u));
+                        const float2 m2 = __ffma2_rn(x2, rlo, magic2);
+                        const float2 h2 = __ffma2_rn(x2, rhi, magic2);
+                        // the two ends differ by a small integer or not at all;
+                        // their squared differences add up exactly, on the FMA
+                        // pipe rather than the busier ALU pipe
+                        const float2 dd = __ffma2_rn(m2, neg1, h2);  // h2 - m2, exact
+                        dacc = __ffma2_rn(dd, dd, dacc);
                         mbits[2 * e] = __float_as_uint(m2.x);  // low byte = code
                         mbits[2 * e + 1] = __float_as_uint(m2.y);
                     }
                     cw[i / 2] = pack_lo_bytes(mbits[0], mbits[1], mbits[2], mbits[3]);
-                    const bool near = (MODE == 0) ? (dacc.x + dacc.y != 0.0f) : (dm >= kNearTie);
-                    fix |= near ? (1u << (i / 2)) : 0u;
+                    flagsf = __fmaf_rn(__fadd_rn(dacc.x, dacc.y), (float)(1u << (3 * (i / 2))), flagsf);
+                }
+                if (flagsf != 0.0f) {  // rare: which groups
+                    const uint32_t u = (uint32_t)flagsf;
+#pragma unroll
+                    for (int q = 0; q < W / 2; ++q) fix |= ((u >> (3 * q)) & 7u) ? (1u << q) : 0u;
                 }
                 // Dynamic mode: the flagged groups (nearly all exact ties,
                 // x/s = n + 1/2) are recomputed in registers by code_exact
@@ -428,7 +461,7 @@ store_kernel(const StoreArgs a) {
                         // with one division where needed, over the codes just stored
                         const uint16_t *src = (kv ? a.v_states : a.k_states) + t * a.x_tok_stride +
                                               (int64_t)h * a.x_head_stride + c * E;
-                        fix_codes<MODE>(src, dst, fix, s_row, r_row, st, rt);
+                        fix_codes<MODE>(src, dst, fix, s_row, r_row, st);
                     }
                 }
             }
@@ -440,7 +473,8 @@ template <int E, int LANES, int MODE, bool V32>
 cudaError_t launch_variant(const StoreArgs &a, cudaStream_t stream) {
     auto kern = store_kernel<E, LANES, MODE, V32>;
     const int C = a.g.head_dim / E;
-    const size_t smem = MODE == 1 ? sizeof(float) * 2 * a.g.kv_heads * C * (E + 2)
+    // mode 1: per (row, lane) chunk, 2E + 4 floats of bracket ends and E + 8 bf16 bounds
+    const size_t smem = MODE == 1 ? (size_t)2 * a.g.kv_heads * C * ((2 * E + 4) * 4 + (E + 8) * 2)
                         : MODE == 0 ? sizeof(float) * 256 : 0;
     static OccupancySlots slots;
     cudaError_t e = cudaSuccess;
