@@ -155,9 +155,10 @@ def test_attention_reports_bad_block():
     check_attention(w, 2, 0.125, qb, got, seqs=[0])  # the other sequence is intact
 
 
-def test_attention_full_size_decode_sampled():
+def test_attention_full_size_decode():
     """The decode batch (256 sequences, contexts up to 8192, 32 query heads on
-    8 kv heads) at full size; 12 sequences checked against the oracle."""
+    8 kv heads) at full size, every sequence and output element checked
+    against the oracle."""
     w = W.decode()
     oracle.store(w.quant_mode, w.k_states, w.v_states, w.k_cache, w.v_cache, w.k_scale,
                  w.v_scale, w.block_table, w.cu_q_lens, w.context_kv_lens)
@@ -165,7 +166,5 @@ def test_attention_full_size_decode_sampled():
     rng = np.random.default_rng(413)
     qb, got, d = run_attention(w, 4, 1.0 / np.sqrt(128), rng, d=d)
     assert d.error_code() == 0
-    order = np.argsort(w.context_lengths)
-    seqs = np.concatenate([order[:4], order[-4:], rng.choice(w.num_seqs, 4, replace=False)])
-    check_attention(w, 4, 1.0 / np.sqrt(128), qb, got, seqs=np.unique(seqs))
+    check_attention(w, 4, 1.0 / np.sqrt(128), qb, got)
     assert not np.any(got == 0xFFFF)
