@@ -28,9 +28,6 @@ int sm_count() {
 namespace {
 
 constexpr int kMaxHeadDim = 256;
-// kv_heads * head_dim of a mode-1 store: its per-channel table (bracket ends and
-// clamp bounds, about 11 bytes per K and V channel) lives in shared memory
-constexpr int64_t kMaxStaticTable = 8192;
 // Appended rows (tokens x 2 x kv_heads) up to which the fused append + gather
 // beats the store followed by a gather (measured on decode-shaped batches:
 // 16 384 rows still won, 65 536 lost).
@@ -117,8 +114,6 @@ kvc8_status kvc8_store(const kvc8_geom *g, int64_t num_tokens, const void *key_s
         !aligned(value_cache, 16))
         return KVC8_ERR_INVALID_ARG;
     if (!aligned(key_scale, 16) || !aligned(value_scale, 16)) return KVC8_ERR_INVALID_ARG;
-    if (g->quant_mode == 1 && (int64_t)g->kv_heads * g->head_dim > kMaxStaticTable)
-        return KVC8_ERR_UNSUPPORTED;
     StoreArgs a;
     a.g = *g;
     a.num_tokens = num_tokens;
@@ -323,8 +318,7 @@ kvc8_status kvc8_append_gather(const kvc8_geom *g, int64_t num_tokens, const voi
     const size_t span_at = plan_bytes(g->num_seqs);
     const bool long_append =
         num_tokens * 2 * g->kv_heads > kFusedAppendMaxRows &&
-        workspace_bytes >= span_at + sizeof(int32_t) * (size_t)g->num_seqs &&
-        !(g->quant_mode == 1 && (int64_t)g->kv_heads * g->head_dim > kMaxStaticTable);
+        workspace_bytes >= span_at + sizeof(int32_t) * (size_t)g->num_seqs;
     if (long_append) {
         StoreArgs s;
         s.g = *g;

@@ -142,9 +142,7 @@ int32_t kvc8_version(void);
  *
  * Tokens whose position leaves the block table or whose block id leaves the
  * pool are skipped and reported through dev_error.  Sequences must not share
- * physical blocks for the slots this call writes.  Mode 1 keeps a table per
- * (K|V, head, channel) in shared memory: kv_heads * head_dim above 8192 gives
- * KVC8_ERR_UNSUPPORTED.
+ * physical blocks for the slots this call writes.
  */
 kvc8_status kvc8_store(const kvc8_geom *g, int64_t num_tokens,
                        const void *key_states, const void *value_states,

@@ -122,6 +122,15 @@ SMALL = [
     # odd block size: the small dynamic-scale gather keeps whole tiles
     dict(q_lens=[20, 1, 9], ctx_before=[6, 13, 0], kv_heads=4, head_dim=64, block_size=7,
          num_blocks=24, quant_mode=0),
+    # static per-channel scales on kv_heads x head_dim = 8448 channels (each
+    # lane keeps its channels' quantities in registers: no table size limit)
+    dict(q_lens=[20, 7], ctx_before=[3, 40], kv_heads=33, head_dim=256, block_size=16,
+         num_blocks=12, quant_mode=1),
+    # one 16-channel lane per row: 30 of a warp's 32 lanes idle
+    dict(q_lens=[9, 1, 30], ctx_before=[0, 7, 2], kv_heads=1, head_dim=16, block_size=4,
+         num_blocks=24, quant_mode=1),
+    dict(q_lens=[9, 1, 30], ctx_before=[0, 7, 2], kv_heads=1, head_dim=16, block_size=4,
+         num_blocks=24, quant_mode=2),
 ]
 
 
@@ -142,6 +151,27 @@ def test_many_sequences(mode):
     w = W.make_workload(f"many{mode}", q_lens=q, ctx_before=ctx, kv_heads=2, head_dim=64,
                         block_size=16, num_blocks=B * 3 + 8, quant_mode=mode, seed=90 + mode)
     check_full(w)
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2])
+def test_strided_input_states(mode):
+    """New K/V rows read through token and head strides wider than the
+    rows (a view into a larger buffer, as from a fused projection)."""
+    w = W.make_workload(f"xstride{mode}", q_lens=[37, 1, 90], ctx_before=[5, 18, 0], kv_heads=4,
+                        head_dim=96, block_size=16, num_blocks=40, quant_mode=mode, seed=95 + mode)
+    d = DeviceBatch(w, fill_out=0xFFFF)
+    N, H, D = w.num_tokens, w.kv_heads, w.head_dim
+    for name in ("k_states", "v_states"):
+        x = getattr(d, name)
+        big = torch.full((N, H + 1, D + 24), 0x7F80, dtype=x.dtype, device=x.device)
+        big[:, :H, :D] = x
+        setattr(d, name, big[:, :H, :D])
+    assert d.k_states.stride() == ((H + 1) * (D + 24), D + 24, 1)
+    d.store()
+    d.gather()
+    assert d.error_code() == 0
+    want_pool = _oracle_store(w)
+    _assert_pool_equal(d.host_caches(), want_pool)
 
 
 def test_strided_padded_output_and_given_offsets():
