@@ -55,6 +55,8 @@
 //
 // Scales whose reciprocal could leave the normal range (and zero scales)
 // always take the exact path.
+#include <type_traits>
+
 #include "kvc8_internal.cuh"
 
 namespace kvc8 {
@@ -192,9 +194,11 @@ constexpr int ring_stages() { return MODE == 1 ? kStagesStatic : kStagesDyn; }
 
 // L lanes per row (a power of two, 32 / L rows per warp), MODE 0 dynamic /
 // 1 static per channel / 2 static per block.
-template <int L, int MODE>
+template <int L, int MODE, bool R32>
 __global__ void __launch_bounds__(kWarpsPerCta * 32, MODE == 1 ? 2 : 4)
 store_kernel(const StoreArgs a) {
+    // cache row indices: 32-bit when the pool has fewer than 2^31 rows
+    using Row = typename std::conditional<R32, int32_t, int64_t>::type;
     constexpr int RW = 32 / L;  // rows per warp
     const int H = a.g.kv_heads, D = a.g.head_dim, bs = a.g.block_size;
     const int B = a.g.num_seqs, MB = a.g.max_blocks_per_seq, NB = a.g.num_blocks;
@@ -234,16 +238,16 @@ store_kernel(const StoreArgs a) {
     const uint16_t *xs = (kv ? a.v_states : a.k_states) + (int64_t)h * a.x_head_stride + c * 16;
     int8_t *cache = (kv ? a.v_cache : a.k_cache) + c * 16;
     float *scl = kv ? a.v_scale : a.k_scale;
-    const int64_t hoff = (int64_t)h * bs;  // cache row of head h in a block, slot 0
+    const Row hoff = (Row)h * bs;  // cache row of head h in a block, slot 0
     const uint32_t my = smem_u32(ring) + ((uint32_t)warp * kStages * 32 + lane) * 32;
 
     // this stream's tokens: s, s + S, s + 2S, ... (all streams together
     // sweep a window of S consecutive tokens through the batch); the rows of
     // its m-th token go to ring slot m % kStages, kStages - 1 tokens ahead
-    const int64_t mine = s < a.num_tokens ? (a.num_tokens - 1 - s) / S + 1 : 0;
+    const int mine = s < a.num_tokens ? (int)((a.num_tokens - 1 - s) / S) + 1 : 0;  // tokens < 2^31
     const int64_t pf_step = (int64_t)S * a.x_tok_stride;
     const uint16_t *pf_src = xs + (int64_t)s * a.x_tok_stride;  // next token to request
-    int64_t pf_left = on ? mine : 0;                              // tokens left to request
+    int pf_left = on ? mine : 0;                                  // tokens left to request
     uint32_t pf_slot = 0;                                         // its ring slot (bytes)
     constexpr uint32_t kRingMask = kStages * 32 * 32 - 1;
     auto prefetch = [&]() {
@@ -291,18 +295,18 @@ store_kernel(const StoreArgs a) {
 
     const float2 magic2 = make_float2(kMagic, kMagic);
     const float2 neg1 = make_float2(-1.0f, -1.0f);
-    int64_t row0 = -1;  // lane i: cache row of (block, head 0, slot) of token 32q + i; -1: skip
+    Row row0 = -1;  // lane i: cache row of (block, head 0, slot) of token 32q + i; -1: skip
     int32_t blk = 0;
     uint32_t rd_slot = 0;  // ring slot of token m (bytes)
 
-    for (int64_t m = 0; m < mine; ++m) {
+    for (int m = 0; m < mine; ++m) {
         const int i = (int)(m & (kChunk - 1));
         if (i == 0) {
             // ---- slots of this stream's next kChunk tokens, one per lane ----
             row0 = -1;
             blk = 0;
             if (m + lane < mine) {
-                const int64_t t = s + (m + lane) * S;
+                const int64_t t = s + (int64_t)(m + lane) * S;
                 int64_t first = t, next = t + 1, ctx;
                 int b;
                 if (a.cu_q_lens != nullptr) {
@@ -336,7 +340,7 @@ store_kernel(const StoreArgs a) {
                     if (blk < 0 || blk >= NB) err = KVC8_DEV_BAD_BLOCK_ID;
                 }
                 if (err == 0) {
-                    row0 = (int64_t)blk * H * bs + (pos - lb * bs);
+                    row0 = (Row)((int64_t)blk * H * bs + (pos - lb * bs));
                 } else {
                     blk = 0;  // never used as an index
                     if (j == 0) report(a.dev_error, err);
@@ -362,21 +366,25 @@ store_kernel(const StoreArgs a) {
         }
         prefetch();
 
-        const int64_t r0 = __shfl_sync(0xFFFFFFFFu, row0, i);
+        const Row r0 = __shfl_sync(0xFFFFFFFFu, row0, i);
         if (r0 < 0) continue;  // warp-uniform: the token is skipped
-        const int64_t drow = r0 + hoff;
+        const Row drow = r0 + hoff;
 
         float s_row = 0.0f, r_row = 0.0f;
         if (MODE == 0) {
             // |x| maximum: max(|a|, |b|) per bf16 half (the sign of the
             // result is garbage and masked off before comparing words)
-            uint32_t m4[4] = {0u, 0u, 0u, 0u};
+            // (a tree: each level takes |.| of the previous maxima again)
+            uint32_t m4[4], m2[2], m1;
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-                asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(m4[k & 3]) : "r"(m4[k & 3]), "r"(w[k]));
-            const uint32_t m2 = __vmaxu2(__vmaxu2(m4[0] & 0x7FFF7FFFu, m4[1] & 0x7FFF7FFFu),
-                                         __vmaxu2(m4[2] & 0x7FFF7FFFu, m4[3] & 0x7FFF7FFFu));
-            uint32_t mag = max(m2 & 0xFFFFu, m2 >> 16);
+            for (int k = 0; k < 4; ++k)
+                asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(m4[k]) : "r"(w[2 * k]), "r"(w[2 * k + 1]));
+#pragma unroll
+            for (int k = 0; k < 2; ++k)
+                asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(m2[k]) : "r"(m4[2 * k]), "r"(m4[2 * k + 1]));
+            asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(m1) : "r"(m2[0]), "r"(m2[1]));
+            m1 &= 0x7FFF7FFFu;
+            uint32_t mag = max(m1 & 0xFFFFu, m1 >> 16);
 #pragma unroll
             for (int o = 1; o < L; o <<= 1)
                 mag = max(mag, __shfl_xor_sync(0xFFFFFFFFu, mag, o));
@@ -476,13 +484,13 @@ store_kernel(const StoreArgs a) {
         }
         if (slow) fix = 0xFu;
         if (on) {
-            int8_t *dst = cache + drow * D;
+            int8_t *dst = cache + (int64_t)drow * D;
             store_codes16(dst, cw);
             if (MODE == 0 && c == 0) scl[drow] = s_row;
             if (fix != 0u) {
                 // rare: the flagged groups of four codes again, one by one,
                 // with one division where needed, over the codes just stored
-                fix_codes<MODE>(xs + (s + m * S) * a.x_tok_stride, dst, fix, s_row, r_row,
+                fix_codes<MODE>(xs + (s + (int64_t)m * S) * a.x_tok_stride, dst, fix, s_row, r_row,
                                 scl + (int64_t)h * D + c * 16);
             }
         }
@@ -490,9 +498,9 @@ store_kernel(const StoreArgs a) {
     cp_async_wait<0>();
 }
 
-template <int L, int MODE>
+template <int L, int MODE, bool R32>
 cudaError_t launch_variant(const StoreArgs &a, cudaStream_t stream) {
-    auto kern = store_kernel<L, MODE>;
+    auto kern = store_kernel<L, MODE, R32>;
     const size_t smem = (MODE == 0 ? sizeof(float) * 256 : 0) + (size_t)kWarpsPerCta * ring_stages<MODE>() * 32 * 32;
     static OccupancySlots slots;
     cudaError_t e = cudaSuccess;
@@ -513,14 +521,20 @@ cudaError_t launch_variant(const StoreArgs &a, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
+template <int MODE, bool R32>
+cudaError_t launch_mode_rows(const StoreArgs &a, cudaStream_t stream) {
+    const int C = a.g.head_dim / 16;  // 1..16
+    if (C <= 1) return launch_variant<1, MODE, R32>(a, stream);
+    if (C <= 2) return launch_variant<2, MODE, R32>(a, stream);
+    if (C <= 4) return launch_variant<4, MODE, R32>(a, stream);
+    if (C <= 8) return launch_variant<8, MODE, R32>(a, stream);
+    return launch_variant<16, MODE, R32>(a, stream);
+}
+
 template <int MODE>
 cudaError_t launch_mode(const StoreArgs &a, cudaStream_t stream) {
-    const int C = a.g.head_dim / 16;  // 1..16
-    if (C <= 1) return launch_variant<1, MODE>(a, stream);
-    if (C <= 2) return launch_variant<2, MODE>(a, stream);
-    if (C <= 4) return launch_variant<4, MODE>(a, stream);
-    if (C <= 8) return launch_variant<8, MODE>(a, stream);
-    return launch_variant<16, MODE>(a, stream);
+    const bool r32 = (int64_t)a.g.num_blocks * a.g.kv_heads * a.g.block_size <= (int64_t)INT32_MAX;
+    return r32 ? launch_mode_rows<MODE, true>(a, stream) : launch_mode_rows<MODE, false>(a, stream);
 }
 
 }  // namespace
