@@ -131,6 +131,11 @@ SMALL = [
          num_blocks=24, quant_mode=1),
     dict(q_lens=[9, 1, 30], ctx_before=[0, 7, 2], kv_heads=1, head_dim=16, block_size=4,
          num_blocks=24, quant_mode=2),
+    # 64 kv heads of 256 channels: a token spans 64 warps, eight CTAs
+    dict(q_lens=[5, 1, 9], ctx_before=[0, 3, 17], kv_heads=64, head_dim=256, block_size=16,
+         num_blocks=8, quant_mode=0),
+    dict(q_lens=[5, 1, 9], ctx_before=[0, 3, 17], kv_heads=64, head_dim=256, block_size=16,
+         num_blocks=8, quant_mode=1),
 ]
 
 
@@ -172,6 +177,32 @@ def test_strided_input_states(mode):
     assert d.error_code() == 0
     want_pool = _oracle_store(w)
     _assert_pool_equal(d.host_caches(), want_pool)
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2])
+def test_pool_declared_beyond_2_31_rows(mode):
+    """A pool declared with more than 2^31 rows (num_blocks * kv_heads *
+    block_size) makes the store index cache rows in 64 bits.  Only the first
+    blocks are allocated, and the block table names only those."""
+    w = W.make_workload(f"rows64_{mode}", q_lens=[37, 1, 50], ctx_before=[3, 20, 0], kv_heads=2,
+                        head_dim=64, block_size=16, num_blocks=40, quant_mode=mode,
+                        seed=120 + mode)
+    d = DeviceBatch(w, fill_out=0xFFFF)
+    d.g.num_blocks = 1 << 27
+    assert d.g.num_blocks * w.kv_heads * w.block_size > 2**31 - 1
+    d.store()
+    d.gather()
+    assert d.error_code() == 0
+    want_pool = _oracle_store(w)
+    _assert_pool_equal(d.host_caches(), want_pool)
+    kc, vc, ks, vs = want_pool
+    ko = np.full((d.out_rows, w.kv_heads, w.head_dim), 0xFFFF, np.uint16)
+    vo = ko.copy()
+    oracle.dequant_gather(w.quant_mode, kc, vc, ks, vs, w.block_table, w.context_lengths, None,
+                          ko, vo)
+    gk, gv = d.host_outputs()
+    _assert_bits_equal(gk, ko, "k_out")
+    _assert_bits_equal(gv, vo, "v_out")
 
 
 def test_strided_padded_output_and_given_offsets():
