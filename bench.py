@@ -36,6 +36,7 @@ import argparse
 import hashlib
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -595,6 +596,25 @@ def path_bytes(w: W.Workload, path: str) -> dict:
     return W.algorithmic_bytes(w)
 
 
+def host_cpu() -> str:
+    """The host CPU as the cpu_baseline reports it: model, architecture, and
+    the cores the OS reports (the oracle itself runs on one)."""
+    model = None
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key, _, val = line.partition(":")
+                key, val = key.strip().lower(), val.strip()
+                if key == "model name":
+                    model = val
+                    break
+                if key == "cpu part" and model is None:
+                    model = {"0xd4f": "Arm Neoverse-V2"}.get(val, "Arm CPU part " + val)
+    except OSError:
+        pass
+    return f"{model or platform.processor() or 'unknown CPU'}, {platform.machine()}, nproc {os.cpu_count()}"
+
+
 def cpu_baseline(w: W.Workload, path: str = "c8", seconds: float = 12.0,
                  per_pass_cap: float = 3.0):
     """The oracle as it stands on one host core, on a bounded sample of the
@@ -618,7 +638,7 @@ def cpu_baseline(w: W.Workload, path: str = "c8", seconds: float = 12.0,
               f"({int(s.q_lens().sum())} stored + {int(s.context_lengths.astype(np.int64).sum())} "
               f"gathered positions, {bytes_pass / 1e6:.1f} MB algorithmic per pass), median pass")
     return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": sample}
+            "sample": sample, "host": host_cpu()}
 
 
 def config_of(args) -> dict:
@@ -654,7 +674,8 @@ def run_reference(args, rank, world):
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": f"each step: oracle store+gather of the first {s.num_seqs} "
                                    f"sequences of the workload ({positions} stored + gathered "
-                                   f"positions, {bytes_step / 1e6:.2f} MB algorithmic)"},
+                                   f"positions, {bytes_step / 1e6:.2f} MB algorithmic)",
+                         "host": host_cpu()},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }

@@ -70,6 +70,7 @@ def test_reference_arm_prints_the_same_config(capsys):
     assert line["impl"] == "reference"
     assert line["config"] == bench.config_of(args)
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["value"] == line["value"]
+    assert "nproc" in line["cpu_baseline"]["host"]
 
 
 def test_traffic_entries_follow_their_kernel_sources(tmp_path, monkeypatch):
