@@ -85,7 +85,7 @@ plan_kernel(const kvc8_geom g, const int32_t *__restrict__ lens,
         carry_tiles_s = 0;
     }
     __syncthreads();
-    for (int base = 0; base < B; base += kPlanThreads) {
+    for (int base = 0; base < B; base += blockDim.x) {
         const int i = base + threadIdx.x;
         int64_t len = 0, span = 0;  // span: output rows of the sequence
         int32_t tiles = 0;
@@ -126,7 +126,7 @@ plan_kernel(const kvc8_geom g, const int32_t *__restrict__ lens,
             if (offsets_out != nullptr) offsets_out[i] = o;
         }
         __syncthreads();
-        if (threadIdx.x == kPlanThreads - 1) {
+        if (threadIdx.x == blockDim.x - 1) {
             carry_len_s = carry_len + inc_len;
             carry_tiles_s = carry_tiles + inc_tiles;
         }
@@ -537,12 +537,18 @@ cudaError_t launch_gather_any(const GatherArgs &a, const AppendArgs &p, bool use
                 : launch_gather_mode<2, false, APPEND>(a, p, use_pdl, stream);
 }
 
+// Threads of the plan's one CTA: a warp per 32 sequences, up to 1024.
+int plan_threads(int32_t num_seqs) {
+    const int w = (num_seqs + 31) / 32;
+    return 32 * (w < 1 ? 1 : (w > kPlanThreads / 32 ? kPlanThreads / 32 : w));
+}
+
 }  // namespace
 
 cudaError_t launch_plan(const kvc8_geom &g, const int32_t *context_lengths,
                         const int64_t *context_seq_offset, int64_t *offsets_out, void *plan,
                         int32_t *dev_error, cudaStream_t stream) {
-    plan_kernel<<<1, kPlanThreads, 0, stream>>>(g, context_lengths, context_seq_offset,
+    plan_kernel<<<1, plan_threads(g.num_seqs), 0, stream>>>(g, context_lengths, context_seq_offset,
                                                 offsets_out, static_cast<char *>(plan), dev_error,
                                                 nullptr, 0, nullptr);
     return cudaGetLastError();
@@ -552,7 +558,7 @@ cudaError_t launch_plan_span(const kvc8_geom &g, const int32_t *context_kv_lens,
                              const int32_t *cu_q_lens, const int64_t *context_seq_offset,
                              void *plan, int32_t *spans_out, int32_t *dev_error,
                              cudaStream_t stream) {
-    plan_kernel<<<1, kPlanThreads, 0, stream>>>(g, context_kv_lens, context_seq_offset, nullptr,
+    plan_kernel<<<1, plan_threads(g.num_seqs), 0, stream>>>(g, context_kv_lens, context_seq_offset, nullptr,
                                                 static_cast<char *>(plan), dev_error, cu_q_lens,
                                                 cu_q_lens != nullptr ? 3 : 4, spans_out);
     return cudaGetLastError();
@@ -562,7 +568,7 @@ cudaError_t launch_plan_append(const kvc8_geom &g, const int32_t *context_kv_len
                                const int32_t *cu_q_lens, const int64_t *context_seq_offset,
                                int64_t *offsets_out, void *plan, int32_t *dev_error,
                                cudaStream_t stream) {
-    plan_kernel<<<1, kPlanThreads, 0, stream>>>(g, context_kv_lens, context_seq_offset,
+    plan_kernel<<<1, plan_threads(g.num_seqs), 0, stream>>>(g, context_kv_lens, context_seq_offset,
                                                 offsets_out, static_cast<char *>(plan), dev_error,
                                                 cu_q_lens, cu_q_lens != nullptr ? 1 : 2, nullptr);
     return cudaGetLastError();
