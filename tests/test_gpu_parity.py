@@ -146,26 +146,26 @@ def test_small_ragged(i):
 
 
 def _random_geometry(i):
-    """Seeded small problem i: head_dim any multiple of 16 up to 256, 1-9 kv
-    heads, block sizes from 1 to 96 (odd ones included), 1-12 sequences with
-    ragged new and cached lengths, all three scale modes, and the decode form
-    (cu_q_lens = None) now and then."""
+    """Seeded small problem i: head_dim any multiple of 16 up to 256, 1-16 kv
+    heads, block sizes from 1 to 128 (odd ones included), 1-39 sequences
+    with ragged new and cached lengths on three scales, all three scale
+    modes, and the decode form (cu_q_lens = None) now and then."""
     rng = np.random.default_rng([4242, i])
     D = 16 * int(rng.integers(1, 17))
-    H = int(rng.integers(1, 10))
-    bs = int(rng.choice([1, 3, 7, 16, 17, 32, 48, 64, 96]))
-    B = int(rng.integers(1, 13))
+    H = int(rng.integers(1, 17))
+    bs = int(rng.choice([1, 2, 3, 5, 7, 8, 16, 17, 31, 32, 48, 64, 96, 128]))
+    B = int(rng.integers(1, 40))
     mode = int(rng.integers(0, 3))
-    decode = bool(rng.random() < 0.25)
-    q = np.ones(B, np.int64) if decode else rng.integers(0, 40, size=B)
-    ctx = rng.integers(0, 90, size=B)
+    decode = bool(rng.random() < 0.2)
+    q = np.ones(B, np.int64) if decode else rng.integers(0, int(rng.choice([3, 40, 300])), size=B)
+    ctx = rng.integers(0, int(rng.choice([5, 100, 1000])), size=B)
     mb = int(((ctx + q + bs - 1) // bs).max())
     return dict(q_lens=q, ctx_before=ctx, kv_heads=H, head_dim=D, block_size=bs,
                 num_blocks=max(B * max(mb, 1) + int(rng.integers(0, 9)), 1), quant_mode=mode,
                 decode_null_cu=decode)
 
 
-@pytest.mark.parametrize("i", range(24))
+@pytest.mark.parametrize("i", range(96))
 def test_random_geometries(i):
     w = W.make_workload(f"rand{i}", seed=300 + i, **_random_geometry(i))
     check_full(w)
