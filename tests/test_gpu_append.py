@@ -14,7 +14,8 @@ import oracle
 import dequant_kvc8_store_gb300 as kv
 from dequant_kvc8_store_gb300 import workloads as W
 from dequant_kvc8_store_gb300.device import DeviceBatch
-from test_gpu_parity import SMALL, _assert_bits_equal, _assert_pool_equal, _oracle_store
+from test_gpu_parity import (SMALL, _assert_bits_equal, _assert_pool_equal, _oracle_store,
+                             _random_geometry)
 
 pytestmark = pytest.mark.gpu
 
@@ -54,6 +55,14 @@ def check_fused(w, *, offsets=None, out_layout="dense", out_pad_rows=0, fill=0xF
 @pytest.mark.parametrize("i", range(len(SMALL)))
 def test_fused_small_ragged(i):
     w = W.make_workload(f"fused{i}", seed=250 + i, **SMALL[i])
+    check_fused(w)
+
+
+@pytest.mark.parametrize("i", range(48))
+def test_fused_random_geometries(i):
+    # the parity file's seeded random problems, through the fused call (its
+    # long appends take the store + plan + gather route)
+    w = W.make_workload(f"frand{i}", seed=600 + i, **_random_geometry(1000 + i))
     check_fused(w)
 
 

@@ -13,6 +13,7 @@ import torch
 import oracle
 import dequant_kvc8_store_gb300 as kv
 from dequant_kvc8_store_gb300 import workloads as W
+from test_gpu_parity import _random_geometry
 
 pytestmark = pytest.mark.gpu
 
@@ -131,6 +132,15 @@ SMALL = [
 @pytest.mark.parametrize("i", range(len(SMALL)))
 def test_bf16_small_ragged(i):
     w = W.make_workload(f"bf16small{i}", seed=150 + i, quant_mode=0, **SMALL[i])
+    check_bf16(w)
+
+
+@pytest.mark.parametrize("i", range(32))
+def test_bf16_random_geometries(i):
+    # the parity file's seeded random problems (scales unused by this path)
+    g = _random_geometry(2000 + i)
+    g["quant_mode"] = 0
+    w = W.make_workload(f"bf16rand{i}", seed=700 + i, **g)
     check_bf16(w)
 
 
