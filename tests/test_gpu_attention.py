@@ -116,6 +116,34 @@ def test_attention_small(i):
     check_attention(w, c["G"], scale, qb, got)
 
 
+def _random_case(i):
+    """Seeded problem i: head_dim 64 or 128, block sizes 16 to 256, 1-8 kv
+    heads with groups of 1-8 query heads, all scale modes, 1-24 sequences
+    whose lengths run from 0 past several 2048-position splits."""
+    rng = np.random.default_rng([5150, i])
+    top = int(rng.choice([40, 600, 9000]))
+    return dict(lens=rng.integers(0, top, size=int(rng.integers(1, 25))),
+                H=int(rng.integers(1, 9)), G=int(rng.integers(1, 9)),
+                D=int(rng.choice([64, 128])), bs=int(rng.choice([16, 32, 48, 64, 128, 256])),
+                mode=int(rng.integers(0, 3)))
+
+
+@pytest.mark.parametrize("i", range(24))
+def test_attention_random(i):
+    c = _random_case(i)
+    lens = np.asarray(c["lens"], np.int64)
+    mb = int(((lens + c["bs"] - 1) // c["bs"]).max()) or 1
+    w = W.make_workload(f"attr{i}", q_lens=np.zeros(len(lens), np.int64), ctx_before=lens,
+                        kv_heads=c["H"], head_dim=c["D"], block_size=c["bs"],
+                        num_blocks=len(lens) * mb + 3, quant_mode=c["mode"], seed=900 + i,
+                        with_store=False)
+    rng = np.random.default_rng(950 + i)
+    scale = 1.0 / np.sqrt(c["D"])
+    qb, got, d = run_attention(w, c["G"], scale, rng)
+    assert d.error_code() == 0
+    check_attention(w, c["G"], scale, qb, got)
+
+
 def test_attention_strided_and_peaked():
     w = W.make_workload("attstr", q_lens=np.zeros(3, np.int64), ctx_before=[700, 2, 1500],
                         kv_heads=4, head_dim=128, block_size=64, num_blocks=80, quant_mode=0,
