@@ -262,6 +262,14 @@ store_kernel(const StoreArgs a) {
     };
 #pragma unroll
     for (int k = 0; k < kStages - 1; ++k) prefetch();
+    // Lanes off the rows feed only the dynamic mode's row maximum, as zeros:
+    // no copy ever lands in their ring slots, so zero those once.
+    if (MODE == 0 && !on) {
+#pragma unroll
+        for (int k = 0; k < 2 * kStages; ++k)
+            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(my + 16 * (k & 1) + 32 * 32 * (k >> 1)), "r"(0u)
+                         : "memory");
+    }
 
     // Static per-channel mode: this lane's bracket ends r_lo, r_hi of
     // r = fl(1/s) and clamp bounds bf16(fl(127 s)) for its 16 channels, held
@@ -358,11 +366,6 @@ store_kernel(const StoreArgs a) {
                          : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]) : "r"(src));
             asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
                          : "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7]) : "r"(src + 16));
-            // lanes off the rows feed only the dynamic mode's row maximum
-            if (MODE == 0 && !on) {
-#pragma unroll
-                for (int k = 0; k < 8; ++k) w[k] = 0u;
-            }
         }
         prefetch();
 
