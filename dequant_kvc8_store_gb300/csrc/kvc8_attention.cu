@@ -76,6 +76,14 @@ __device__ __forceinline__ float2 dequant2(uint32_t w, int e0, int e1, float s0,
     return __fmul2_rn(x, make_float2(s0, s1));
 }
 
+// 2^x by the hardware approximation (relative error far below the bf16
+// rounding the weights get next); -inf gives 0.
+__device__ __forceinline__ float ex2_fast(float x) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
 __device__ __forceinline__ float bf16_lo(uint32_t x) { return __uint_as_float(x << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t x) { return __uint_as_float(x & 0xFFFF0000u); }
 
@@ -222,11 +230,11 @@ __device__ __forceinline__ void compute_tile(const AttnArgs &a, int h, const flo
         x1 = fmaxf(x1, __shfl_xor_sync(0xFFFFFFFFu, x1, sh));
     }
     const float n0 = fmaxf(m0, x0), n1 = fmaxf(m1, x1);  // finite: valid >= 1
-    const float corr0 = exp2f(m0 - n0), corr1 = exp2f(m1 - n1);
+    const float corr0 = ex2_fast(m0 - n0), corr1 = ex2_fast(m1 - n1);
     m0 = n0;
     m1 = n1;
-    const uint32_t plo = pack_bf16(exp2f(c[0] - n0), exp2f(c[1] - n1));  // position gid
-    const uint32_t phi = pack_bf16(exp2f(c[2] - n0), exp2f(c[3] - n1));  // position gid+8
+    const uint32_t plo = pack_bf16(ex2_fast(c[0] - n0), ex2_fast(c[1] - n1));  // position gid
+    const uint32_t phi = pack_bf16(ex2_fast(c[2] - n0), ex2_fast(c[3] - n1));  // position gid+8
     l0 = l0 * corr0 + (bf16_lo(plo) + bf16_lo(phi));
     l1 = l1 * corr1 + (bf16_hi(plo) + bf16_hi(phi));
 #pragma unroll
